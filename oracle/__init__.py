@@ -1,0 +1,14 @@
+"""CPU oracle of the DSA forward step (test infrastructure only).
+
+Only the test suite, the smoke check and the benchmark's CPU-baseline leg
+import this package; the CUDA library never does.
+"""
+from .dsa_oracle import (  # noqa: F401
+    additive_mask_row,
+    dsa_decode,
+    dsa_prefill,
+    index_scores,
+    index_scores_row,
+    masked_attention_row,
+    topk_select,
+)

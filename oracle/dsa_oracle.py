@@ -1,0 +1,280 @@
+"""CPU oracle for the DeepSeek Sparse Attention (DSA) forward step.
+
+TEST INFRASTRUCTURE ONLY.  This module is the slow, plainly written
+definition that the CUDA library is checked against.  Only the test suite,
+the smoke check and the benchmark's CPU-baseline leg may import it; the
+library itself never calls it and has no CPU fallback.
+
+Everything here is numpy in float64.  Inputs arrive as whatever the caller
+generated (fp32 or bf16 values); they are widened exactly to float64 before
+any arithmetic.  Nothing is blocked, fused or reordered beyond what the
+definitions below state.
+
+Sources (transformers model documentation pages):
+
+* "DeepSeek-V3.2" page, section "DeepSeek Sparse Attention (DSA)":
+  - the Lightning Indexer computes an index score between each query and
+    all previous keys with a light, few-head module; the port computes it
+    directly in bf16/fp32 (the FP8 + Hadamard form of the original code is
+    only a precision optimisation because the rotation is orthogonal);
+  - fine-grained token selection keeps the ``index_topk`` most relevant
+    tokens per query (2048 by default) and the main MLA attention is then
+    computed only over those tokens *through an additive mask*;
+  - the indexer keeps its own single-head key cache of ``index_head_dim``
+    per token next to the K/V cache;
+  - each layer runs its own indexer (no sharing of the selection).
+* "DeepSeek-V3.2" page, ``DeepseekV32Config`` parameters: ``index_topk``
+  (2048), ``index_head_dim`` (128), ``index_n_heads`` (64),
+  ``kv_lora_rank`` (512), ``qk_rope_head_dim`` (64), ``qk_nope_head_dim``
+  (128), ``num_attention_heads`` (128).
+* "DeepSeek-V4" page, section on the attention-mask layout: an indexer slot
+  with no selection is marked by a ``-1`` pointer.
+
+The exact indexer formula is not printed on the pages.  The reading used
+here is  I[t,s] = sum_j w[t,j] * ReLU(q_I[t,j,:] . k_I[s,:])  for s <= t,
+with no extra scale; every other open point is listed with its reading in
+the repository's design notes.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "index_scores_row",
+    "index_scores",
+    "topk_select",
+    "additive_mask_row",
+    "masked_attention_row",
+    "dsa_prefill",
+    "dsa_decode",
+]
+
+_NEG_INF = -np.inf
+
+
+def _f64(x):
+    """Widen an fp32 / bf16 / fp64 array (numpy or torch) to float64 exactly."""
+    try:  # torch tensors (bf16 has no numpy dtype): go through float32
+        import torch  # noqa: WPS433
+
+        if isinstance(x, torch.Tensor):
+            return x.detach().to("cpu", torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Step 1: Lightning Indexer scores
+# --------------------------------------------------------------------------
+def index_scores_row(q_idx_t, w_t, k_idx_prefix):
+    """Index scores of one query against every key at or before it.
+
+    DeepSeek-V3.2 page, "DeepSeek Sparse Attention (DSA)", Lightning Indexer
+    paragraph: a score between the query and all previous keys, computed by
+    ``index_n_heads`` light heads of width ``index_head_dim`` against a
+    single-head key cache.  Reading:  I[s] = sum_j w[j] * max(0, q[j,:].k[s,:]).
+
+    q_idx_t:      [H_I, D_I]   indexer query heads of this token
+    w_t:          [H_I]        per-head weights of this token
+    k_idx_prefix: [n, D_I]     indexer keys of positions 0..n-1 (n = t+1)
+    returns       [n] float64
+    """
+    q = _f64(q_idx_t)
+    w = _f64(w_t)
+    k = _f64(k_idx_prefix)
+    dots = q @ k.T                      # [H_I, n]: q_I[t,j] . k_I[s]
+    return w @ np.maximum(dots, 0.0)    # sum over heads of w_j * ReLU(dot)
+
+
+def index_scores(q_idx, w, k_idx):
+    """Full causal score matrix of one sequence.
+
+    q_idx [L, H_I, D_I], w [L, H_I], k_idx [L, D_I]  ->  I [L, L] float64,
+    with -inf where s > t (keys after the query are not "previous keys").
+    """
+    q = _f64(q_idx)
+    L = q.shape[0]
+    out = np.full((L, L), _NEG_INF)
+    for t in range(L):
+        out[t, : t + 1] = index_scores_row(q[t], _f64(w[t]), _f64(k_idx[: t + 1]))
+    return out
+
+
+# --------------------------------------------------------------------------
+# Step 2: per-query top-k selection
+# --------------------------------------------------------------------------
+def topk_select(scores, k):
+    """Indices of the ``k`` most relevant tokens of one query.
+
+    DeepSeek-V3.2 page, "DeepSeek Sparse Attention (DSA)", fine-grained token
+    selection paragraph: keep the ``index_topk`` most relevant tokens.  When
+    fewer than ``k`` candidates exist every candidate is kept.  Ties are
+    broken toward the lower position (order = score descending, then
+    position ascending); -0.0 and +0.0 are the same score.  The kept
+    positions are returned in ascending order, padded with -1 (the
+    DeepSeek-V4 page's marker for an empty indexer slot) to length ``k``.
+
+    scores: [n] scores of candidate positions 0..n-1 (n = t+1)
+    returns int64 [k]
+    """
+    s = _f64(scores)
+    n = s.shape[0]
+    keep = min(k, n)
+    # A stable sort on the negated score puts larger scores first and keeps
+    # equal scores in ascending position order.
+    order = np.argsort(-s, kind="stable")[:keep]
+    out = np.full(k, -1, dtype=np.int64)
+    out[:keep] = np.sort(order)
+    return out
+
+
+# --------------------------------------------------------------------------
+# Steps 3-4: additive mask and MLA attention (absorbed latent form)
+# --------------------------------------------------------------------------
+def additive_mask_row(selected, L):
+    """Row of the additive mask: 0 at selected positions, -inf elsewhere.
+
+    DeepSeek-V3.2 page, "DeepSeek Sparse Attention (DSA)": the main MLA
+    attention is computed only over the selected tokens via an additive
+    mask.  Positions after the query are never selected, so the causal
+    mask is contained in this one.
+    """
+    m = np.full(L, _NEG_INF)
+    sel = np.asarray(selected)
+    sel = sel[sel >= 0]
+    m[sel] = 0.0
+    return m
+
+
+def masked_attention_row(q_t, kv, mask_row, scale, d_v):
+    """Dense softmax attention of one query over all L keys plus the mask.
+
+    Absorbed MLA form: each of the H heads has a query of width D_qk
+    (kv_lora_rank latent + qk_rope_head_dim rope part, 512 + 64 at the
+    DeepSeek-V3.2 configuration); all heads share one key row of width D_qk
+    and the value is the first d_v (= kv_lora_rank) columns of that row.
+
+    z[h,s] = scale * q[h,:].kv[s,:] + mask[s];  p = softmax_s(z);
+    O[h,:] = sum_s p[h,s] kv[s,:d_v];  lse[h] = log sum_s exp(z[h,s]).
+
+    q_t [H, D_qk], kv [L, D_qk], mask_row [L]  ->  (O [H, d_v], lse [H])
+    """
+    q = _f64(q_t)
+    k = _f64(kv)
+    z = scale * (q @ k.T) + mask_row[None, :]          # [H, L]
+    zmax = np.max(z, axis=1, keepdims=True)
+    e = np.exp(z - zmax)                               # exp(-inf) = 0
+    denom = np.sum(e, axis=1, keepdims=True)
+    p = e / denom
+    out = p @ k[:, :d_v]
+    lse = (zmax + np.log(denom))[:, 0]
+    return out, lse
+
+
+# --------------------------------------------------------------------------
+# The whole forward step
+# --------------------------------------------------------------------------
+def _one_query(q_idx_t, w_t, k_idx_seq, q_t, kv_seq, t, topk, scale, d_v):
+    """Steps 1-4 for the query at sequence position t (0-based)."""
+    scores = index_scores_row(q_idx_t, w_t, k_idx_seq[: t + 1])
+    sel = topk_select(scores, topk)
+    L = kv_seq.shape[0]
+    mask = additive_mask_row(sel, L)
+    out, lse = masked_attention_row(q_t, kv_seq, mask, scale, d_v)
+    return scores, sel, out, lse
+
+
+def dsa_prefill(q_idx, w, k_idx, q, kv, cu_seqlens, topk, scale, d_v, rows=None):
+    """DSA forward over a packed batch of causal sequences.
+
+    Packed ("varlen") layout: sequence b owns rows cu_seqlens[b] ..
+    cu_seqlens[b+1]-1 of every input; positions are sequence-local and
+    every sequence is causal on its own.
+
+    q_idx [T, H_I, D_I], w [T, H_I], k_idx [T, D_I], q [T, H, D_qk],
+    kv [T, D_qk], cu_seqlens [B+1].
+
+    rows: optional iterable of global row numbers to evaluate (the oracle
+    is O(L) per row; long inputs are checked on a sample).  Default: all.
+
+    Returns a dict with, for the evaluated rows (in the order given):
+      rows   [R] int64 global rows
+      pos    [R] int64 sequence-local positions
+      scores list of [pos+1] float64 arrays (index scores of the row)
+      idx    [R, topk] int64 selected positions (ascending, -1 padded)
+      out    [R, H, d_v] float64
+      lse    [R, H] float64
+    """
+    cu = [int(c) for c in np.asarray(cu_seqlens).reshape(-1)]
+    T = cu[-1]
+    if rows is None:
+        rows = range(T)
+    rows = [int(r) for r in rows]
+    seq_of = np.searchsorted(np.asarray(cu), np.asarray(rows, dtype=np.int64), side="right") - 1
+    H = q.shape[1]
+    res_pos, res_scores, res_idx = [], [], []
+    res_out = np.zeros((len(rows), H, d_v))
+    res_lse = np.zeros((len(rows), H))
+    cache = {}
+    for i, (r, b) in enumerate(zip(rows, seq_of)):
+        b = int(b)
+        lo, hi = cu[b], cu[b + 1]
+        if b not in cache:  # widen each sequence's shared tensors once
+            cache = {b: (_f64(k_idx[lo:hi]), _f64(kv[lo:hi]))}
+        k_seq, kv_seq = cache[b]
+        t = r - lo
+        sc, sel, o, l = _one_query(_f64(q_idx[r]), _f64(w[r]), k_seq, _f64(q[r]), kv_seq, t, topk, scale, d_v)
+        res_pos.append(t)
+        res_scores.append(sc)
+        res_idx.append(sel)
+        res_out[i] = o
+        res_lse[i] = l
+    return {
+        "rows": np.asarray(rows, dtype=np.int64),
+        "pos": np.asarray(res_pos, dtype=np.int64),
+        "scores": res_scores,
+        "idx": np.asarray(res_idx, dtype=np.int64).reshape(len(rows), topk),
+        "out": res_out,
+        "lse": res_lse,
+    }
+
+
+def dsa_decode(q_idx, w, q, idx_cache, kv_cache, cache_seqlens, topk, scale, d_v, batches=None):
+    """DSA forward for one new query per sequence over its caches.
+
+    DeepSeek-V3.2 page, "DeepSeek Sparse Attention (DSA)": the indexer keeps
+    its own single-head key cache (``index_head_dim`` per token) beside the
+    main K/V cache and is updated before it is read.  Reading: the caches
+    already hold the new token, so ``cache_seqlens[b]`` counts it and the
+    query sits at position cache_seqlens[b]-1; every cached position is a
+    candidate.
+
+    q_idx [B, H_I, D_I], w [B, H_I], q [B, H, D_qk],
+    idx_cache [B, max_ctx, D_I], kv_cache [B, max_ctx, D_qk], cache_seqlens [B].
+    Returns dict(batches, scores (list), idx [R, topk], out [R,H,d_v], lse [R,H]).
+    """
+    lens = [int(n) for n in np.asarray(cache_seqlens).reshape(-1)]
+    if batches is None:
+        batches = range(len(lens))
+    batches = [int(b) for b in batches]
+    H = q.shape[1]
+    res_scores, res_idx = [], []
+    res_out = np.zeros((len(batches), H, d_v))
+    res_lse = np.zeros((len(batches), H))
+    for i, b in enumerate(batches):
+        n = lens[b]
+        k_seq = _f64(idx_cache[b, :n])
+        kv_seq = _f64(kv_cache[b, :n])
+        sc, sel, o, l = _one_query(_f64(q_idx[b]), _f64(w[b]), k_seq, _f64(q[b]), kv_seq, n - 1, topk, scale, d_v)
+        res_scores.append(sc)
+        res_idx.append(sel)
+        res_out[i] = o
+        res_lse[i] = l
+    return {
+        "batches": np.asarray(batches, dtype=np.int64),
+        "scores": res_scores,
+        "idx": np.asarray(res_idx, dtype=np.int64).reshape(len(batches), topk),
+        "out": res_out,
+        "lse": res_lse,
+    }
