@@ -1,0 +1,419 @@
+"""Benchmark of the DSA forward step on B300.
+
+Workload (default): long prefill, B=1, L=32768, indexer 64 heads x 128,
+index_topk 2048, MLA 128 heads, 576/512, bf16, seeded synthetic inputs.
+One step = one pass of the whole path: Lightning Indexer -> top-k ->
+sparse MLA attention (the kernels dsa_forward launches, called stage by
+stage so that each kernel is timed with CUDA events on its stream).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 (under torchrun): every rank runs its own independent problem of the
+same size (weak scaling, no collective on the data path); the time is the
+max over ranks.  --impl reference times the CPU oracle (numpy fp64) on a
+bounded sample of query rows of the same workload.
+
+Prints ONE JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSA fwd queries/s and TFLOP/s per stage at L=32K, as % of B300 roofline"
+FLOP_PER_PAIR_IDX = 2 * 64 * 128            # indexer, per causal (t, s) pair
+FLOP_PER_PAIR_ATTN = 2 * 128 * (576 + 512)  # attention, per selected (t, s) pair
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _workload_desc(cfg, lens):
+    return (f"{cfg.name} prefill: B={len(lens)}, L={max(lens)} causal, indexer {cfg.n_idx_heads}x{cfg.idx_dim}, "
+            f"index_topk={cfg.topk}, MLA {cfg.n_heads} heads {cfg.d_qk}/{cfg.d_v}, {cfg.dtype}")
+
+
+def _work_counts(lens, k):
+    causal = sum(L * (L + 1) // 2 for L in lens)
+    selected = sum(sum(min(k, t + 1) for t in range(L)) for L in lens)
+    return causal, selected
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    def __init__(self, index, path):
+        self.path = path
+        self.proc = None
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(cfg, inp_cpu, rows):
+    """Time the CPU oracle on the given rows; returns (seconds, rows)."""
+    import oracle.dsa_oracle as O
+
+    t0 = time.perf_counter()
+    O.dsa_prefill(inp_cpu["q_idx"], inp_cpu["w"], inp_cpu["k_idx"], inp_cpu["q"], inp_cpu["kv"],
+                  inp_cpu["cu_seqlens"], cfg.topk, cfg.softmax_scale, cfg.d_v, rows=rows)
+    return time.perf_counter() - t0
+
+
+def _sample_rows(L, k, n_extra, seed):
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    base = [0, k - 2, k - 1, k, L - 1]
+    extra = [int(x) for x in rng.integers(0, L, size=n_extra)]
+    return sorted(set(t for t in base + extra if 0 <= t < L))
+
+
+def _host_copy_for_oracle(inp, rows):
+    """Host copies the oracle needs: whole k_I / kv, and only the sampled rows of the per-query tensors."""
+    import torch
+
+    T = inp["q"].shape[0]
+    out = {"k_idx": inp["k_idx"].cpu(), "kv": inp["kv"].cpu(), "cu_seqlens": inp["cu_seqlens"].cpu()}
+    for name in ("q_idx", "w", "q"):
+        src = inp[name]
+        full = torch.zeros((T,) + tuple(src.shape[1:]), dtype=src.dtype) if False else None
+        sub = src[rows].cpu()
+        out[name] = _RowView(sub, rows)
+    return out
+
+
+class _RowView:
+    """Row-indexable view of a few host rows of a large device tensor (oracle input)."""
+
+    def __init__(self, sub, rows):
+        self.sub = sub
+        self.pos = {r: i for i, r in enumerate(rows)}
+        self.shape = (None,) + tuple(sub.shape[1:])
+
+    def __getitem__(self, r):
+        return self.sub[self.pos[int(r)]]
+
+
+def run_reference(args, cfg):
+    """--impl reference: the CPU oracle, as it stands, on a bounded sample of rows per step."""
+    import torch
+
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from sparse_attention_long_gemm_b300.synth import make_prefill_inputs
+
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    inp = make_prefill_inputs(cfg, dev, seed=0)
+    L = inp["max_seqlen"]
+    rows_per_step = args.ref_rows
+    rows = _sample_rows(L, cfg.topk, 4 * rows_per_step, seed=1)
+    host = _host_copy_for_oracle(inp, rows)
+    del inp
+    import numpy as np
+
+    rng = np.random.default_rng(2)
+    times, done = [], 0
+    for i in range(args.warmup + args.steps):
+        step_rows = sorted(rng.choice(rows, size=min(rows_per_step, len(rows)), replace=False).tolist())
+        dt = oracle_sample(cfg, host, step_rows)
+        if i >= args.warmup:
+            times.append(dt)
+            done += len(step_rows)
+    total = sum(times)
+    v = done / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "queries/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": _workload_desc(cfg, [L]), "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": v, "unit": "queries/s", "cores": _cpu_cores(), "kind": "oracle",
+                         "sample": f"{rows_per_step} query rows per step drawn from positions {rows[:8]}..."
+                                   f" (t in {{0,k-2,k-1,k,L-1}} + uniform), dense additive-mask oracle"},
+        "e2e": {"value": v, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_attention_long_gemm_b300 as dsa
+    from sparse_attention_long_gemm_b300.build import build_library
+    from sparse_attention_long_gemm_b300.synth import make_prefill_inputs
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build_library()
+    if ws > 1:
+        dist.barrier()
+    p = dsa.params_from_config(cfg)
+    inp = make_prefill_inputs(cfg, dev, seed=rank)   # weak scaling: one independent problem per rank
+    lens = inp["lengths"]
+    T = sum(lens)
+    B = len(lens)
+    maxL = inp["max_seqlen"]
+    ld = (maxL + 3) // 4 * 4
+    causal, selected = _work_counts(lens, cfg.topk)
+    scores = torch.empty((T, ld), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, cfg.topk), dtype=torch.int32, device=dev)
+    out = torch.empty((T, cfg.n_heads, cfg.d_v), dtype=inp["q"].dtype, device=dev)
+    lse = torch.empty((T, cfg.n_heads), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (126 MB)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        dsa.dsa_index_scores(p, inp["q_idx"], inp["w"], inp["k_idx"], inp["cu_seqlens"], B, T, maxL, scores, ld, sp)
+        if evs:
+            evs[1].record(stream)
+        dsa.dsa_topk(p, scores, ld, inp["cu_seqlens"], B, T, maxL, idx, sp)
+        if evs:
+            evs[2].record(stream)
+        dsa.dsa_sparse_mla_attn(p, inp["q"], inp["kv"], idx, inp["cu_seqlens"], B, T, maxL, out, lse, sp)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    err = dsa.dsa_get_device_error(sp)
+    if err != 0:
+        raise RuntimeError(f"device error during warm-up: {err}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
+        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, f"/tmp/dsa_clocks_{rank}.csv")
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    for s in range(args.steps):
+        flush.zero_()          # L2 flushed between steps (not inside the timed events)
+        step(evs[s])
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    err = dsa.dsa_get_device_error(sp)
+    if err != 0:
+        raise RuntimeError(f"device error during timing: {err}")
+    st = [[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs]
+    step_ms = sum(sum(x) for x in st) / args.steps
+    stage_ms = [sum(x[i] for x in st) / args.steps for i in range(3)]
+    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    step_ms_max = float(t.item())
+
+    # ---- end to end: host buffers, H2D + fused dsa_forward + D2H inside the timed region ----
+    e2e = None
+    if not args.no_e2e:
+        names = ["q_idx", "w", "k_idx", "q", "kv", "cu_seqlens"]
+        host = {n: inp[n].cpu().pin_memory() for n in names}
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dev_in = {n: torch.empty_like(inp[n]) for n in names}
+        del inp
+        wsb = torch.empty(dsa.dsa_workspace_size(p, T, maxL, B), dtype=torch.uint8, device=dev)
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = h_out.numel() * h_out.element_size()
+
+        def e2e_step():
+            for n in names:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            dsa.dsa_forward(p, dev_in["q_idx"], dev_in["w"], dev_in["k_idx"], dev_in["q"], dev_in["kv"],
+                            dev_in["cu_seqlens"], B, T, maxL, out, None, None, wsb, sp)
+            h_out.copy_(out, non_blocking=True)
+
+        for _ in range(max(1, min(args.warmup, 2))):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        ne = max(2, min(args.steps, 5))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if ws > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(ne):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = torch.tensor([e0.elapsed_time(e1) / ne], dtype=torch.float64, device=dev)
+        if ws > 1:
+            dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
+        e2e = {"value": T * ws / (float(e_ms.item()) / 1e3), "unit": "queries/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": ne}
+        if dsa.dsa_get_device_error(sp) != 0:
+            raise RuntimeError("device error during the end-to-end loop")
+
+    if rank != 0:
+        if ws > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    peaks = _peaks()
+    idx_tf = causal * FLOP_PER_PAIR_IDX / (stage_ms[0] * 1e-3) / 1e12
+    topk_bytes = causal * 4 + T * cfg.topk * 4
+    topk_gbs = topk_bytes / (stage_ms[1] * 1e-3) / 1e9
+    attn_tf = selected * FLOP_PER_PAIR_ATTN / (stage_ms[2] * 1e-3) / 1e12
+    peak_t = peaks["bf16_tflops_sustained"]
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            traffic = json.load(f).get("attn_tc_kernel_long")
+    except (OSError, ValueError):
+        traffic = None
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, args)
+    line = {
+        "metric": METRIC,
+        "value": T * ws / (step_ms_max / 1e3),
+        "unit": "queries/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": _workload_desc(cfg, lens), "l2": "flushed (256 MB write) between timed steps",
+                   "per_rank": "independent problem per rank (seed = rank)"},
+        "stages": {
+            "index_scores": {"ms": stage_ms[0], "tflops": idx_tf, "frac_of_peak": idx_tf / peak_t},
+            "topk": {"ms": stage_ms[1], "gbs": topk_gbs, "frac_of_peak": topk_gbs / peaks["hbm_gbs"]},
+            "sparse_mla_attn": {"ms": stage_ms[2], "tflops": attn_tf, "frac_of_peak": attn_tf / peak_t},
+        },
+        "roofline": {"bound": "tensor", "kernel": "attn_tc_kernel", "achieved": attn_tf, "peak": peak_t,
+                     "unit": "TFLOP/s", "frac": attn_tf / peak_t, "traffic": traffic,
+                     "peak_kind": f"bf16 dense, sustained, {peaks['source']}",
+                     "frac_of_burst": attn_tf / peaks["bf16_tflops"]},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": 3 * args.steps,
+        "path": dsa.dsa_path_name(p),
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def cpu_baseline(cfg, args):
+    """The oracle as it stands on the host cores, on a bounded sample of the same workload."""
+    import torch
+
+    from sparse_attention_long_gemm_b300.synth import make_prefill_inputs
+
+    inp = make_prefill_inputs(cfg, "cuda:0", seed=0)
+    L = inp["max_seqlen"]
+    rows = _sample_rows(L, cfg.topk, args.cpu_rows, seed=1)
+    host = _host_copy_for_oracle(inp, rows)
+    del inp
+    torch.cuda.empty_cache()
+    dt = oracle_sample(cfg, host, rows)
+    return {"value": len(rows) / dt, "unit": "queries/s", "cores": _cpu_cores(), "kind": "oracle",
+            "sample": f"{len(rows)} query rows of the same workload (t in {{0,k-2,k-1,k,L-1}} + uniform), "
+                      f"{dt:.1f} s of CPU work"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="long")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=24)
+    ap.add_argument("--ref-rows", type=int, default=6)
+    args = ap.parse_args()
+    from sparse_attention_long_gemm_b300.synth import CONFIGS
+
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

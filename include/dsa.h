@@ -1,0 +1,198 @@
+/*
+ * dsa.h -- C ABI of libdsa: the DeepSeek Sparse Attention (DSA) forward step
+ * on one NVIDIA B300 (sm_103a).
+ *
+ * What is computed (transformers model documentation, "DeepSeek-V3.2" page,
+ * section "DeepSeek Sparse Attention (DSA)"; sizes from its DeepseekV32Config
+ * parameters):
+ *
+ *   1. Lightning Indexer.  A light module with n_idx_heads (index_n_heads)
+ *      heads of width idx_dim (index_head_dim) scores each query t against
+ *      every key s at or before it, over a single-head indexer key cache:
+ *          I[t,s] = sum_j w[t,j] * max(0, q_idx[t,j,:] . k_idx[s,:]),  s <= t.
+ *      (The pages give the ingredients; this exact form, with no extra
+ *      scale, is the reading used throughout.)
+ *   2. Fine-grained token selection.  For each query keep the topk
+ *      (index_topk) highest-scoring positions; when t+1 <= topk every
+ *      position 0..t is kept.  Equal scores go to the lower position;
+ *      -0.0 equals +0.0.
+ *   3. Main MLA attention over the selected positions only, in the absorbed
+ *      latent form: each of n_heads heads has a d_qk-wide query (latent
+ *      kv_lora_rank + rope qk_rope_head_dim: 512 + 64); all heads share the
+ *      d_qk-wide key row kv[s,:] and the value is its first d_v columns.
+ *      This equals the pages' additive-mask formulation (0 on selected
+ *      positions, -inf elsewhere) because exp(-inf) = 0.
+ *          z[h,i] = softmax_scale * q[t,h,:] . kv[s_i,:]
+ *          out[t,h,:] = sum_i softmax(z[h,:])_i kv[s_i, 0:d_v]
+ *          lse[t,h]   = log sum_i exp(z[h,i])          (natural log)
+ *   Each layer runs its own indexer (no state is kept between calls).
+ *
+ * Conventions common to every entry point
+ *   - Memory: every pointer argument is DEVICE memory owned by the caller,
+ *     except `const dsa_params*` (host).  The library allocates nothing;
+ *     scratch for the fused calls is the caller's `workspace`.
+ *   - Streams: work is enqueued asynchronously on `stream` (a cudaStream_t;
+ *     NULL = legacy default stream).  Nothing synchronises the host.
+ *   - Layout: row-major, last dimension contiguous, no padding except where
+ *     a leading dimension (`ld`) is passed.  Tensor base addresses must be
+ *     16-byte aligned.
+ *   - Types: q_idx, k_idx, q, kv, caches and out have the element type
+ *     `params->dtype` (DSA_BF16 or DSA_FP32); w, scores and lse are float32;
+ *     cu_seqlens, cache_seqlens and selected indices are int32.
+ *   - Packed ("varlen") batches: sequence b owns rows cu_seqlens[b] ..
+ *     cu_seqlens[b+1]-1 of every per-token tensor; cu_seqlens[0] = 0,
+ *     non-decreasing, cu_seqlens[batch] = total_q.  Positions are
+ *     sequence-local and each sequence is causal on its own.  A single
+ *     sequence is batch = 1, cu_seqlens = {0, L}.
+ *   - Selected indices are sequence-local positions in ascending order,
+ *     padded with -1 to topk entries (the DeepSeek-V4 page's marker for an
+ *     empty indexer slot).
+ *   - Errors: every call returns DSA_OK (0) or a negative status and never
+ *     aborts the process.  Argument errors are detected on the host before
+ *     anything is enqueued.  Errors that can only be seen on the device
+ *     (non-monotone cu_seqlens, cache_seqlens outside [1, max_ctx], a
+ *     bounded wait that ran out) make the kernels skip the affected work and
+ *     raise a device error word that dsa_get_device_error() reports.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define DSA_OK               0
+#define DSA_ERR_ARG         -1  /* null pointer, non-positive size, bad dtype */
+#define DSA_ERR_SHAPE       -2  /* inconsistent sizes (ld < max_seqlen, ...)  */
+#define DSA_ERR_UNSUPPORTED -3  /* a size outside the supported limits        */
+#define DSA_ERR_CUDA        -4  /* a CUDA runtime call failed                 */
+#define DSA_ERR_TIMEOUT     -5  /* a bounded device-side wait ran out         */
+#define DSA_ERR_WORKSPACE   -6  /* workspace pointer null or too small        */
+#define DSA_ERR_DEVICE_DATA -7  /* device-side check of cu_seqlens / cache_seqlens failed */
+
+/* element types */
+#define DSA_BF16 0
+#define DSA_FP32 1
+
+/* Problem description (host struct, read during the call only).
+ * DeepSeek-V3.2 values: n_idx_heads 64, idx_dim 128, n_heads 128,
+ * d_qk 576, d_v 512, topk 2048, softmax_scale 1/sqrt(192), DSA_BF16. */
+typedef struct dsa_params {
+    int   n_idx_heads;    /* H_I: indexer heads (index_n_heads)              */
+    int   idx_dim;        /* D_I: indexer head width (index_head_dim)        */
+    int   n_heads;        /* H: attention heads (num_attention_heads)        */
+    int   d_qk;           /* query/key width: latent + rope                  */
+    int   d_v;            /* value width: the latent (kv_lora_rank), <= d_qk */
+    int   topk;           /* k: tokens kept per query (index_topk)           */
+    float softmax_scale;  /* multiplies q.kv before the softmax              */
+    int   dtype;          /* DSA_BF16 or DSA_FP32                            */
+} dsa_params;
+
+/* Limits: 1 <= n_idx_heads <= 128, 8 <= idx_dim <= 256 (multiple of 8),
+ * 1 <= n_heads <= 256, 8 <= d_v <= d_qk <= 1024 (multiples of 8),
+ * 1 <= topk <= 16384, max_seqlen / max_ctx <= 1048576.
+ * The tensor-core path is taken for the DeepSeek-V3.2 shape in bf16
+ * (64, 128, 128, 576, 512); other shapes run the general kernels. */
+
+/* Human-readable name of a status code (static string). */
+const char* dsa_status_string(int status);
+
+/* Bytes of `workspace` that dsa_forward needs: the fp32 index-score rows
+ * (total_q x round_up(max_seqlen, 4)) plus, when the caller passes no
+ * idx_out, the selected-index rows (total_q x topk int32), each 256-byte
+ * aligned.  Returns 0 for invalid arguments. */
+size_t dsa_workspace_size(const dsa_params* params, int total_q, int max_seqlen, int batch);
+
+/* Bytes of `workspace` that dsa_forward_decode needs (score rows of
+ * batch x round_up(max_ctx, 4) floats, plus index rows when idx_out is
+ * NULL).  Returns 0 for invalid arguments. */
+size_t dsa_decode_workspace_size(const dsa_params* params, int batch, int max_ctx);
+
+/* Step 1 (Lightning Indexer) over a packed batch.
+ *   q_idx  [total_q, n_idx_heads, idx_dim]   dtype
+ *   w      [total_q, n_idx_heads]            float32
+ *   k_idx  [total_q, idx_dim]                dtype (indexer key cache)
+ *   cu_seqlens [batch+1]                     int32 (device)
+ *   scores [total_q, ld] float32, written for s <= t only (row r holds the
+ *          scores of the query at global row r against positions 0..t of
+ *          its sequence); entries s > t are left untouched.
+ *   ld >= max_seqlen, ld a multiple of 4; max_seqlen >= every length. */
+int dsa_index_scores(const dsa_params* params, const void* q_idx, const float* w,
+                     const void* k_idx, const int* cu_seqlens, int batch, int total_q,
+                     int max_seqlen, float* scores, long long ld, void* stream);
+
+/* Step 2 (top-k) over score rows laid out as dsa_index_scores writes them.
+ * Row r (position t in its sequence) selects among scores[r*ld + 0..t].
+ *   idx [total_q, topk] int32: ascending positions, -1 padded.
+ * Bit-exact: the same score array always gives the same indices. */
+int dsa_topk(const dsa_params* params, const float* scores, long long ld,
+             const int* cu_seqlens, int batch, int total_q, int max_seqlen,
+             int* idx, void* stream);
+
+/* Step 3 (sparse MLA attention) over given selections.
+ *   q   [total_q, n_heads, d_qk]  dtype
+ *   kv  [total_q, d_qk]           dtype (latent + rope key rows)
+ *   idx [total_q, topk]           int32, sequence-local, ascending, -1 padded;
+ *                                 entry i valid iff i < min(topk, t+1)
+ *   out [total_q, n_heads, d_v]   dtype
+ *   lse [total_q, n_heads]        float32, or NULL */
+int dsa_sparse_mla_attn(const dsa_params* params, const void* q, const void* kv,
+                        const int* idx, const int* cu_seqlens, int batch, int total_q,
+                        int max_seqlen, void* out, float* lse, void* stream);
+
+/* Steps 1-3 fused over a packed prefill batch.  Arguments as above;
+ * idx_out [total_q, topk] may be NULL (then the indices live in workspace).
+ * workspace: device memory of at least dsa_workspace_size(...) bytes,
+ * 256-byte aligned, not used concurrently by another call. */
+int dsa_forward(const dsa_params* params, const void* q_idx, const float* w,
+                const void* k_idx, const void* q, const void* kv,
+                const int* cu_seqlens, int batch, int total_q, int max_seqlen,
+                void* out, float* lse, int* idx_out,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Steps 1-3 for one new query per sequence over its caches (decode).
+ *   q_idx [batch, n_idx_heads, idx_dim], w [batch, n_idx_heads],
+ *   q [batch, n_heads, d_qk]
+ *   idx_cache [batch, max_ctx, idx_dim]   indexer key cache, dtype
+ *   kv_cache  [batch, max_ctx, d_qk]      latent + rope cache, dtype
+ *   cache_seqlens [batch] int32 (device): valid cache length INCLUDING the
+ *          new token (the caches are updated first); the query sits at
+ *          position cache_seqlens[b]-1 and every cached position is a
+ *          candidate.  1 <= cache_seqlens[b] <= max_ctx.
+ *   out [batch, n_heads, d_v], lse [batch, n_heads] or NULL,
+ *   idx_out [batch, topk] or NULL (cache positions, -1 padded). */
+int dsa_forward_decode(const dsa_params* params, const void* q_idx, const float* w,
+                       const void* q, const void* idx_cache, const void* kv_cache,
+                       const int* cache_seqlens, int batch, int max_ctx,
+                       void* out, float* lse, int* idx_out,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device error word:
+ * DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_DATA (DSA_ERR_CUDA if the
+ * synchronisation itself failed). */
+int dsa_get_device_error(void* stream);
+
+/* Upper bound, in nanoseconds, of every spin-wait inside the kernels
+ * (default 2e9).  After it runs out a kernel raises DSA_ERR_TIMEOUT in the
+ * device error word and returns instead of hanging.  Returns the previous
+ * value.  Values < 1000 are clamped to 1000. */
+long long dsa_set_wait_timeout_ns(long long ns);
+
+/* Self-test of the bounded-wait path: enqueues a one-block kernel that
+ * waits on an mbarrier no thread ever arrives at, with a timeout of
+ * `timeout_ns`.  A correct library returns DSA_OK from this call and
+ * DSA_ERR_TIMEOUT from the next dsa_get_device_error(stream). */
+int dsa_selftest_wait_timeout(long long timeout_ns, void* stream);
+
+/* Name of the kernel family a call with these parameters runs:
+ * "tcgen05" (sm_103a tensor-core kernels) or "simt" (general kernels). */
+const char* dsa_path_name(const dsa_params* params);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif  /* DSA_H_ */

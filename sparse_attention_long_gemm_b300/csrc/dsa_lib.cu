@@ -1,0 +1,376 @@
+// dsa_lib.cu -- the C ABI of libdsa (declared in include/dsa.h).
+//
+// Host side only: argument validation, tensor-map construction for TMA,
+// choice between the tensor-core kernels (DeepSeek-V3.2 shape, bf16) and the
+// general CUDA-core kernels, and asynchronous launches on the caller's
+// stream.  Nothing here allocates device memory or synchronises, except
+// dsa_get_device_error which is documented to synchronise.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "attn_simt.cuh"
+#include "attn_tc.cuh"
+#include "indexer_simt.cuh"
+#include "indexer_tc.cuh"
+#include "topk.cuh"
+
+using namespace dsa;
+
+namespace {
+
+std::atomic<long long> g_timeout_ns{2000000000LL};
+
+// prefill indexer: 4 queries (256 MMA columns) per block, 3 key stages, 2 query buffers
+constexpr int kPreNQ = 4, kPreKS = 3, kPreQB = 2, kPreKC = 32;
+// decode indexer: 1 query (64 columns), 5 key stages, 2 query buffers
+constexpr int kDecNQ = 1, kDecKS = 5, kDecQB = 2, kDecKC = 8;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+
+bool is_tc_shape(const dsa_params* p) {
+    return p->dtype == DSA_BF16 && p->n_idx_heads == kIdxHeads && p->idx_dim == kIdxDim && p->n_heads == kAttnHeads &&
+           p->d_qk == kAttnDqk && p->d_v == kAttnDv;
+}
+
+int check_params(const dsa_params* p) {
+    if (p == nullptr) return DSA_ERR_ARG;
+    if (p->dtype != DSA_BF16 && p->dtype != DSA_FP32) return DSA_ERR_ARG;
+    if (p->n_idx_heads < 1 || p->idx_dim < 1 || p->n_heads < 1 || p->d_qk < 1 || p->d_v < 1 || p->topk < 1)
+        return DSA_ERR_ARG;
+    if (!std::isfinite(p->softmax_scale)) return DSA_ERR_ARG;
+    if (p->n_idx_heads > 128 || p->idx_dim > 256 || p->idx_dim % 8 != 0 || p->n_idx_heads * p->idx_dim > 16384)
+        return DSA_ERR_UNSUPPORTED;
+    if (p->n_heads > 256 || p->d_qk > 1024 || p->d_v > p->d_qk || p->d_qk % 8 != 0 || p->d_v % 8 != 0 || p->d_v < 8)
+        return DSA_ERR_UNSUPPORTED;
+    if (p->topk > 16384) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return DSA_OK;
+    return DSA_ERR_CUDA;
+}
+
+int launch_status() { return cuda_status(cudaGetLastError()); }
+
+struct DevInfo {
+    int sm_count = 0;
+    bool attrs_set = false;
+};
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+int device_info(DevInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo& d = g_dev[dev];
+    if (!d.attrs_set) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSA_ERR_CUDA;
+        cudaError_t e = cudaSuccess;
+        auto set = [&](const void* fn, size_t bytes) {
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+        };
+        set(reinterpret_cast<const void*>(&indexer_tc_kernel<kPreNQ, kPreKS, kPreQB>), IdxTc<kPreNQ, kPreKS, kPreQB>::SMEM);
+        set(reinterpret_cast<const void*>(&indexer_tc_kernel<kDecNQ, kDecKS, kDecQB>), IdxTc<kDecNQ, kDecKS, kDecQB>::SMEM);
+        set(reinterpret_cast<const void*>(&attn_tc_kernel), AttnTc::SMEM);
+        set(reinterpret_cast<const void*>(&indexer_simt_kernel<float>), indexer_simt_smem(128, 128));
+        set(reinterpret_cast<const void*>(&indexer_simt_kernel<__nv_bfloat16>), indexer_simt_smem(128, 128));
+        set(reinterpret_cast<const void*>(&attn_simt_kernel<float>), attn_simt_smem(1024, 16384));
+        set(reinterpret_cast<const void*>(&attn_simt_kernel<__nv_bfloat16>), attn_simt_smem(1024, 16384));
+        if (e != cudaSuccess) return DSA_ERR_CUDA;
+        d.attrs_set = true;
+    }
+    *out = &d;
+    return DSA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (row stride = cols elements), box [box_rows, 64]
+// with 128-byte swizzle: each box row is one 128-byte swizzle row.
+int make_tmap_bf16(CUtensorMap* tm, const void* base, long long rows, long long cols, int box_rows) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return DSA_ERR_CUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// stage launchers (arguments already validated)
+// ---------------------------------------------------------------------------
+int run_index_scores(const dsa_params* p, const void* q_idx, const float* w, const void* k_idx, const RowSpec& rs,
+                     int rows, long long key_rows, float* scores, long long ld, cudaStream_t st) {
+    DevInfo* di = nullptr;
+    int rc = device_info(&di);
+    if (rc != DSA_OK) return rc;
+    const unsigned long long to = static_cast<unsigned long long>(g_timeout_ns.load());
+    if (is_tc_shape(p) && rs.batch <= kIdxTcMaxBatch) {
+        CUtensorMap tq, tk;
+        if (!rs.decode) {
+            using C = IdxTc<kPreNQ, kPreKS, kPreQB>;
+            if ((rc = make_tmap_bf16(&tq, q_idx, static_cast<long long>(rows) * kIdxHeads, kIdxDim, C::BN)) != DSA_OK)
+                return rc;
+            if ((rc = make_tmap_bf16(&tk, k_idx, key_rows, kIdxDim, kIdxTileKeys)) != DSA_OK) return rc;
+            indexer_tc_kernel<kPreNQ, kPreKS, kPreQB>
+                <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, rs, w, scores, ld, kPreKC, to);
+        } else {
+            using C = IdxTc<kDecNQ, kDecKS, kDecQB>;
+            if ((rc = make_tmap_bf16(&tq, q_idx, static_cast<long long>(rows) * kIdxHeads, kIdxDim, C::BN)) != DSA_OK)
+                return rc;
+            if ((rc = make_tmap_bf16(&tk, k_idx, key_rows, kIdxDim, kIdxTileKeys)) != DSA_OK) return rc;
+            indexer_tc_kernel<kDecNQ, kDecKS, kDecQB>
+                <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, rs, w, scores, ld, kDecKC, to);
+        }
+        return launch_status();
+    }
+    const size_t sm = indexer_simt_smem(p->n_idx_heads, p->idx_dim);
+    if (p->dtype == DSA_BF16)
+        indexer_simt_kernel<__nv_bfloat16><<<rows, kIdxSimtThreads, sm, st>>>(
+            rs, static_cast<const __nv_bfloat16*>(q_idx), w, static_cast<const __nv_bfloat16*>(k_idx), p->n_idx_heads,
+            p->idx_dim, scores, ld);
+    else
+        indexer_simt_kernel<float><<<rows, kIdxSimtThreads, sm, st>>>(rs, static_cast<const float*>(q_idx), w,
+                                                                      static_cast<const float*>(k_idx),
+                                                                      p->n_idx_heads, p->idx_dim, scores, ld);
+    return launch_status();
+}
+
+int run_topk(const dsa_params* p, const float* scores, long long ld, const RowSpec& rs, int rows, int* idx,
+             cudaStream_t st) {
+    topk_kernel<<<rows, kTopkThreads, 0, st>>>(rs, scores, ld, p->topk, idx);
+    return launch_status();
+}
+
+int run_attn(const dsa_params* p, const void* q, const void* kv, const int* idx, const RowSpec& rs, int rows,
+             void* out, float* lse, cudaStream_t st) {
+    DevInfo* di = nullptr;
+    int rc = device_info(&di);
+    if (rc != DSA_OK) return rc;
+    if (is_tc_shape(p)) {
+        CUtensorMap tq;
+        if ((rc = make_tmap_bf16(&tq, q, static_cast<long long>(rows) * kAttnHeads, kAttnDqk, kAttnHeads)) != DSA_OK)
+            return rc;
+        const float scale_log2 = p->softmax_scale * 1.4426950408889634f;
+        attn_tc_kernel<<<2 * rows, kAttnThreads, AttnTc::SMEM, st>>>(
+            tq, static_cast<const __nv_bfloat16*>(kv), idx, rs, p->topk, scale_log2,
+            static_cast<__nv_bfloat16*>(out), lse, static_cast<unsigned long long>(g_timeout_ns.load()));
+        return launch_status();
+    }
+    const dim3 grid(rows, p->n_heads);
+    const size_t sm = attn_simt_smem(p->d_qk, p->topk);
+    if (p->dtype == DSA_BF16)
+        attn_simt_kernel<__nv_bfloat16><<<grid, kAttnSimtThreads, sm, st>>>(
+            rs, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kv), idx, p->topk,
+            p->n_heads, p->d_qk, p->d_v, p->softmax_scale, static_cast<__nv_bfloat16*>(out), lse);
+    else
+        attn_simt_kernel<float><<<grid, kAttnSimtThreads, sm, st>>>(
+            rs, static_cast<const float*>(q), static_cast<const float*>(kv), idx, p->topk, p->n_heads, p->d_qk,
+            p->d_v, p->softmax_scale, static_cast<float*>(out), lse);
+    return launch_status();
+}
+
+int check_prefill_common(const dsa_params* p, const int* cu, int batch, int total_q, int max_seqlen) {
+    int rc = check_params(p);
+    if (rc != DSA_OK) return rc;
+    if (cu == nullptr || batch < 1 || total_q < 0 || max_seqlen < 1) return DSA_ERR_ARG;
+    if (max_seqlen > (1 << 20)) return DSA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(total_q) * p->n_heads * p->d_qk > (1LL << 40)) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_string(int status) {
+    switch (status) {
+        case DSA_OK: return "DSA_OK";
+        case DSA_ERR_ARG: return "DSA_ERR_ARG: null pointer, non-positive size or bad dtype";
+        case DSA_ERR_SHAPE: return "DSA_ERR_SHAPE: inconsistent sizes";
+        case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED: size outside the supported limits";
+        case DSA_ERR_CUDA: return "DSA_ERR_CUDA: a CUDA runtime call failed";
+        case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT: a bounded device-side wait ran out";
+        case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE: workspace missing or too small";
+        case DSA_ERR_DEVICE_DATA: return "DSA_ERR_DEVICE_DATA: cu_seqlens / cache_seqlens / indices out of range";
+        default: return "unknown dsa status";
+    }
+}
+
+const char* dsa_path_name(const dsa_params* params) {
+    if (check_params(params) != DSA_OK) return "invalid";
+    return is_tc_shape(params) ? "tcgen05" : "simt";
+}
+
+size_t dsa_workspace_size(const dsa_params* params, int total_q, int max_seqlen, int batch) {
+    if (check_params(params) != DSA_OK || total_q < 0 || max_seqlen < 1 || batch < 1) return 0;
+    const long long ld = round_up(max_seqlen, 4);
+    const long long sc = round_up(static_cast<long long>(total_q) * ld * 4, 256);
+    const long long ix = round_up(static_cast<long long>(total_q) * params->topk * 4, 256);
+    return static_cast<size_t>(sc + ix);
+}
+
+size_t dsa_decode_workspace_size(const dsa_params* params, int batch, int max_ctx) {
+    if (check_params(params) != DSA_OK || batch < 1 || max_ctx < 1) return 0;
+    const long long ld = round_up(max_ctx, 4);
+    const long long sc = round_up(static_cast<long long>(batch) * ld * 4, 256);
+    const long long ix = round_up(static_cast<long long>(batch) * params->topk * 4, 256);
+    return static_cast<size_t>(sc + ix);
+}
+
+int dsa_index_scores(const dsa_params* params, const void* q_idx, const float* w, const void* k_idx,
+                     const int* cu_seqlens, int batch, int total_q, int max_seqlen, float* scores, long long ld,
+                     void* stream) {
+    int rc = check_prefill_common(params, cu_seqlens, batch, total_q, max_seqlen);
+    if (rc != DSA_OK) return rc;
+    if (q_idx == nullptr || w == nullptr || k_idx == nullptr || scores == nullptr) return DSA_ERR_ARG;
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(scores)) return DSA_ERR_ARG;
+    if (ld < max_seqlen || ld % 4 != 0) return DSA_ERR_SHAPE;
+    if (total_q == 0) return DSA_OK;
+    const RowSpec rs{cu_seqlens, batch, 0, max_seqlen};
+    return run_index_scores(params, q_idx, w, k_idx, rs, total_q, total_q, scores, ld,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int dsa_topk(const dsa_params* params, const float* scores, long long ld, const int* cu_seqlens, int batch,
+             int total_q, int max_seqlen, int* idx, void* stream) {
+    int rc = check_prefill_common(params, cu_seqlens, batch, total_q, max_seqlen);
+    if (rc != DSA_OK) return rc;
+    if (scores == nullptr || idx == nullptr) return DSA_ERR_ARG;
+    if (!aligned16(scores) || !aligned16(idx)) return DSA_ERR_ARG;
+    if (ld < max_seqlen || ld % 4 != 0) return DSA_ERR_SHAPE;
+    if (total_q == 0) return DSA_OK;
+    const RowSpec rs{cu_seqlens, batch, 0, max_seqlen};
+    return run_topk(params, scores, ld, rs, total_q, idx, static_cast<cudaStream_t>(stream));
+}
+
+int dsa_sparse_mla_attn(const dsa_params* params, const void* q, const void* kv, const int* idx,
+                        const int* cu_seqlens, int batch, int total_q, int max_seqlen, void* out, float* lse,
+                        void* stream) {
+    int rc = check_prefill_common(params, cu_seqlens, batch, total_q, max_seqlen);
+    if (rc != DSA_OK) return rc;
+    if (q == nullptr || kv == nullptr || idx == nullptr || out == nullptr) return DSA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(idx) || !aligned16(out) || (lse && !aligned16(lse)))
+        return DSA_ERR_ARG;
+    if (total_q == 0) return DSA_OK;
+    const RowSpec rs{cu_seqlens, batch, 0, max_seqlen};
+    return run_attn(params, q, kv, idx, rs, total_q, out, lse, static_cast<cudaStream_t>(stream));
+}
+
+int dsa_forward(const dsa_params* params, const void* q_idx, const float* w, const void* k_idx, const void* q,
+                const void* kv, const int* cu_seqlens, int batch, int total_q, int max_seqlen, void* out, float* lse,
+                int* idx_out, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_prefill_common(params, cu_seqlens, batch, total_q, max_seqlen);
+    if (rc != DSA_OK) return rc;
+    if (q_idx == nullptr || w == nullptr || k_idx == nullptr || q == nullptr || kv == nullptr || out == nullptr)
+        return DSA_ERR_ARG;
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(q) || !aligned16(kv) ||
+        !aligned16(out) || (lse && !aligned16(lse)) || (idx_out && !aligned16(idx_out)))
+        return DSA_ERR_ARG;
+    if (total_q == 0) return DSA_OK;
+    const size_t need = dsa_workspace_size(params, total_q, max_seqlen, batch);
+    if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return DSA_ERR_WORKSPACE;
+    const long long ld = round_up(max_seqlen, 4);
+    float* scores = static_cast<float*>(workspace);
+    int* idx = idx_out ? idx_out
+                       : reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                                round_up(static_cast<long long>(total_q) * ld * 4, 256));
+    const RowSpec rs{cu_seqlens, batch, 0, max_seqlen};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((rc = run_index_scores(params, q_idx, w, k_idx, rs, total_q, total_q, scores, ld, st)) != DSA_OK) return rc;
+    if ((rc = run_topk(params, scores, ld, rs, total_q, idx, st)) != DSA_OK) return rc;
+    return run_attn(params, q, kv, idx, rs, total_q, out, lse, st);
+}
+
+int dsa_forward_decode(const dsa_params* params, const void* q_idx, const float* w, const void* q,
+                       const void* idx_cache, const void* kv_cache, const int* cache_seqlens, int batch, int max_ctx,
+                       void* out, float* lse, int* idx_out, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_params(params);
+    if (rc != DSA_OK) return rc;
+    if (q_idx == nullptr || w == nullptr || q == nullptr || idx_cache == nullptr || kv_cache == nullptr ||
+        cache_seqlens == nullptr || out == nullptr || batch < 1 || max_ctx < 1)
+        return DSA_ERR_ARG;
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(q) || !aligned16(idx_cache) || !aligned16(kv_cache) ||
+        !aligned16(out) || (lse && !aligned16(lse)) || (idx_out && !aligned16(idx_out)))
+        return DSA_ERR_ARG;
+    if (max_ctx > (1 << 20)) return DSA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(batch) * max_ctx > (1LL << 31) / 64) return DSA_ERR_UNSUPPORTED;
+    const size_t need = dsa_decode_workspace_size(params, batch, max_ctx);
+    if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return DSA_ERR_WORKSPACE;
+    const long long ld = round_up(max_ctx, 4);
+    float* scores = static_cast<float*>(workspace);
+    int* idx = idx_out ? idx_out
+                       : reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                                round_up(static_cast<long long>(batch) * ld * 4, 256));
+    const RowSpec rs{cache_seqlens, batch, 1, max_ctx};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long key_rows = static_cast<long long>(batch) * max_ctx;
+    if ((rc = run_index_scores(params, q_idx, w, idx_cache, rs, batch, key_rows, scores, ld, st)) != DSA_OK) return rc;
+    if ((rc = run_topk(params, scores, ld, rs, batch, idx, st)) != DSA_OK) return rc;
+    return run_attn(params, q, kv_cache, idx, rs, batch, out, lse, st);
+}
+
+int dsa_get_device_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess) return DSA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) return DSA_ERR_CUDA;
+    return v;
+}
+
+long long dsa_set_wait_timeout_ns(long long ns) {
+    if (ns < 1000) ns = 1000;
+    return g_timeout_ns.exchange(ns);
+}
+
+}  // extern "C"
+
+namespace dsa {
+// one thread waits on an mbarrier that nothing arrives at
+__global__ void selftest_wait_kernel(unsigned long long timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        wait_bar(smem_u32(&bar), 0, timeout_ns, &abort_flag);
+    }
+}
+}  // namespace dsa
+
+extern "C" int dsa_selftest_wait_timeout(long long timeout_ns, void* stream) {
+    if (timeout_ns < 1000) timeout_ns = 1000;
+    if (timeout_ns > 10000000000LL) return DSA_ERR_ARG;
+    dsa::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<unsigned long long>(timeout_ns));
+    return launch_status();
+}

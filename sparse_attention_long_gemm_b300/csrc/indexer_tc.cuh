@@ -1,0 +1,314 @@
+// indexer_tc.cuh -- Lightning Indexer on the sm_103a tensor cores.
+//
+// DeepSeek-V3.2 page, "DeepSeek Sparse Attention (DSA)", Lightning Indexer,
+// at the DeepseekV32Config sizes index_n_heads = 64, index_head_dim = 128:
+//     I[t,s] = sum_j w[t,j] * max(0, q_I[t,j,:] . k_I[s,:])   for s <= t.
+//
+// The contraction is computed transposed, S^T = k_I . q_I^T: a tile of 128
+// keys is the MMA's M (one TMEM lane per key) and NQ queries x 64 heads its
+// N, K = 128.  Each epilogue thread then owns one key and sums its 64 heads
+// for each query in registers (ReLU and the w-weighted head sum fused), so
+// the per-head scores never leave TMEM and no cross-lane reduction is
+// needed.  Only the causal part (s <= t) is computed and written.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over work units):
+//   warp 0      TMA producer: query block (NQ*64 rows x 128, once per unit)
+//               and key tiles (128 x 128) into 128B-swizzled shared memory;
+//   warp 1      allocates TMEM and issues tcgen05.mma (one thread);
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, ReLU, w-sum,
+//               coalesced fp32 stores of the score rows.
+// Two TMEM accumulators alternate so the epilogue of one key tile overlaps
+// the MMAs of the next.
+//
+// Work unit = (query block of NQ consecutive queries of one sequence, a run
+// of at most `kc` key tiles).  Bounding the run length keeps every unit
+// about the same size, so a static round-robin over CTAs balances the
+// causal triangle (and, in decode, long caches) without sorting.
+#pragma once
+
+#include <cuda.h>
+
+#include "rows.cuh"
+
+namespace dsa {
+
+constexpr int kIdxHeads = 64;
+constexpr int kIdxDim = 128;
+constexpr int kIdxTileKeys = 128;
+constexpr int kIdxTcThreads = 192;
+constexpr int kIdxTcMaxBatch = 256;
+
+template <int NQ, int KSTAGES, int QBUF>
+struct IdxTc {
+    static constexpr int BN = NQ * kIdxHeads;                 // MMA N
+    static constexpr int Q_BYTES = BN * kIdxDim * 2;          // one query block
+    static constexpr int Q_HALF = BN * 128;                   // 64 columns (128 B) of it
+    static constexpr int K_BYTES = kIdxTileKeys * kIdxDim * 2;
+    static constexpr int K_HALF = kIdxTileKeys * 128;
+    static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+    static constexpr int OFF_K = QBUF * Q_BYTES;
+    static constexpr int OFF_BAR = OFF_K + KSTAGES * K_BYTES;
+    static constexpr int NBAR = 2 * QBUF + 2 * KSTAGES + 4 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int OFF_TABLE = OFF_MISC + 16;
+    static constexpr int SMEM = OFF_TABLE + (kIdxTcMaxBatch + 1) * 4 + 1024;  // + alignment slack
+    static constexpr uint32_t IDESC = idesc_bf16(128, BN, false, false);
+};
+
+struct IdxUnit {
+    int q_row0;          // global row of the block's first query
+    int nq;              // valid queries in the block (1..NQ)
+    int t0;              // sequence position of the first query
+    long long key_base;  // key-tensor row of position 0
+    int kt0, kt1;        // key tiles [kt0, kt1)
+};
+
+// number of chunks of key tiles for a query block in causal band m
+__device__ __forceinline__ int idx_chunks(int m, int kc) { return (m + kc) / kc; }   // ceil((m+1)/kc)
+// sum over bands m' < M of idx_chunks(m')
+__device__ __forceinline__ long long idx_chunks_below(int M, int kc) {
+    const long long a = M / kc, rr = M % kc;
+    return kc * a * (a + 1) / 2 + rr * (a + 1);
+}
+
+template <int NQ>
+struct IdxSched {
+    static constexpr int QPB = kIdxTileKeys / NQ;   // query blocks per band of 128 positions
+
+    // units before query block q of a sequence
+    __device__ __forceinline__ static long long units_before(int q, int kc) {
+        const int band = q / QPB;
+        return QPB * idx_chunks_below(band, kc) + static_cast<long long>(q - band * QPB) * idx_chunks(band, kc);
+    }
+    // units of sequence b (0 when its length is invalid)
+    __device__ static long long seq_units(const RowSpec& rs, int b, int kc) {
+        if (rs.decode) {
+            const int n = __ldg(rs.lens + b);
+            if (n < 1 || n > rs.max_len) { raise_error(DSA_ERR_DEVICE_DATA); return 0; }
+            const int ntiles = (n + kIdxTileKeys - 1) / kIdxTileKeys;
+            return (ntiles + kc - 1) / kc;
+        }
+        const int lo = __ldg(rs.lens + b), hi = __ldg(rs.lens + b + 1);
+        const int len = hi - lo;
+        if (lo < 0 || len < 0 || len > rs.max_len) { raise_error(DSA_ERR_DEVICE_DATA); return 0; }
+        const int nqb = (len + NQ - 1) / NQ;
+        return units_before(nqb, kc);
+    }
+    // unit v of sequence b
+    __device__ static IdxUnit unit(const RowSpec& rs, int b, long long v, int kc) {
+        IdxUnit U;
+        if (rs.decode) {
+            const int n = __ldg(rs.lens + b);
+            const int ntiles = (n + kIdxTileKeys - 1) / kIdxTileKeys;
+            U.q_row0 = b;
+            U.nq = 1;
+            U.t0 = n - 1;
+            U.key_base = static_cast<long long>(b) * rs.max_len;
+            U.kt0 = static_cast<int>(v) * kc;
+            U.kt1 = min(U.kt0 + kc, ntiles);
+            return U;
+        }
+        const int lo = __ldg(rs.lens + b), len = __ldg(rs.lens + b + 1) - lo;
+        const int nqb = (len + NQ - 1) / NQ;
+        int ql = 0, qh = nqb - 1;   // largest q with units_before(q) <= v
+        while (ql < qh) {
+            const int mid = (ql + qh + 1) >> 1;
+            if (units_before(mid, kc) <= v) ql = mid; else qh = mid - 1;
+        }
+        const int c = static_cast<int>(v - units_before(ql, kc));
+        const int band = ql / QPB;
+        U.t0 = ql * NQ;
+        U.nq = min(NQ, len - U.t0);
+        U.q_row0 = lo + U.t0;
+        U.key_base = lo;
+        U.kt0 = c * kc;
+        U.kt1 = min(U.kt0 + kc, band + 1);
+        return U;
+    }
+};
+
+template <int NQ, int KSTAGES, int QBUF>
+__global__ void __launch_bounds__(kIdxTcThreads, 1)
+indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, RowSpec rs,
+                  const float* __restrict__ w, float* __restrict__ scores, long long ld, int kc,
+                  unsigned long long timeout_ns) {
+    using C = IdxTc<NQ, KSTAGES, QBUF>;
+    using Sch = IdxSched<NQ>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase, sK = sbase + C::OFF_K;
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    auto q_full = [&](int i) { return bar0 + 8u * i; };
+    auto q_empty = [&](int i) { return bar0 + 8u * (QBUF + i); };
+    auto k_full = [&](int i) { return bar0 + 8u * (2 * QBUF + i); };
+    auto k_empty = [&](int i) { return bar0 + 8u * (2 * QBUF + KSTAGES + i); };
+    auto acc_full = [&](int i) { return bar0 + 8u * (2 * QBUF + 2 * KSTAGES + i); };
+    auto acc_empty = [&](int i) { return bar0 + 8u * (2 * QBUF + 2 * KSTAGES + 2 + i); };
+    const uint32_t done_bar = bar0 + 8u * (2 * QBUF + 2 * KSTAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    int* s_pref = reinterpret_cast<int*>(smem + C::OFF_TABLE);   // units before sequence b
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int i = 0; i < QBUF; ++i) { mbar_init(q_full(i), 1); mbar_init(q_empty(i), 1); }
+        for (int i = 0; i < KSTAGES; ++i) { mbar_init(k_full(i), 1); mbar_init(k_empty(i), 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(acc_full(i), 1); mbar_init(acc_empty(i), 128); }
+        mbar_init(done_bar, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    // per-sequence unit prefix (serial; the batch is small on this path)
+    if (tid == 32 * 2) {
+        long long acc = 0;
+        for (int b = 0; b < rs.batch; ++b) {
+            s_pref[b] = static_cast<int>(acc);
+            acc += Sch::seq_units(rs, b, kc);
+        }
+        s_pref[rs.batch] = static_cast<int>(acc);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total_units = s_pref[rs.batch];
+
+    auto get_unit = [&](int u) {
+        int bl = 0, bh = rs.batch - 1;
+        while (bl < bh) {
+            const int mid = (bl + bh + 1) >> 1;
+            if (s_pref[mid] <= u) bl = mid; else bh = mid - 1;
+        }
+        return Sch::unit(rs, bl, u - s_pref[bl], kc);
+    };
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        int it_q = 0, it_k = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            const IdxUnit U = get_unit(u);
+            const int qb = it_q % QBUF;
+            ok = wait_bar(q_empty(qb), ((it_q / QBUF) & 1) ^ 1, timeout_ns, s_abort);
+            if (!ok) break;
+            mbar_expect_tx(q_full(qb), C::Q_BYTES);
+            for (int kh = 0; kh < 2; ++kh)
+                tma_load_2d(sQ + qb * C::Q_BYTES + kh * C::Q_HALF, &tm_q, kh * 64, U.q_row0 * kIdxHeads, q_full(qb));
+            for (int kt = U.kt0; kt < U.kt1; ++kt) {
+                const int s = it_k % KSTAGES;
+                ok = wait_bar(k_empty(s), ((it_k / KSTAGES) & 1) ^ 1, timeout_ns, s_abort);
+                if (!ok) break;
+                mbar_expect_tx(k_full(s), C::K_BYTES);
+                const int krow = static_cast<int>(U.key_base + static_cast<long long>(kt) * kIdxTileKeys);
+                for (int kh = 0; kh < 2; ++kh)
+                    tma_load_2d(sK + s * C::K_BYTES + kh * C::K_HALF, &tm_k, kh * 64, krow, k_full(s));
+                ++it_k;
+            }
+            ++it_q;
+        }
+        if (!ok) sleep_ns(2000000ull);  // let copies already issued land before the CTA exits
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        int it_q = 0, it_k = 0, it_acc = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            const IdxUnit U = get_unit(u);
+            const int qb = it_q % QBUF;
+            ok = wait_bar(q_full(qb), (it_q / QBUF) & 1, timeout_ns, s_abort);
+            if (!ok) break;
+            tc_fence_after();
+            for (int kt = U.kt0; kt < U.kt1; ++kt) {
+                const int s = it_k % KSTAGES;
+                const int ab = it_acc & 1;
+                ok = wait_bar(k_full(s), (it_k / KSTAGES) & 1, timeout_ns, s_abort) &&
+                     wait_bar(acc_empty(ab), ((it_acc >> 1) & 1) ^ 1, timeout_ns, s_abort);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(ab * C::BN);
+#pragma unroll
+                for (int kh = 0; kh < 2; ++kh) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = sdesc_sw128(sK + s * C::K_BYTES + kh * C::K_HALF + kk * 32, 16, 1024);
+                        const uint64_t b = sdesc_sw128(sQ + qb * C::Q_BYTES + kh * C::Q_HALF + kk * 32, 16, 1024);
+                        tc_mma_bf16(d, a, b, C::IDESC, (kh | kk) ? 1u : 0u);
+                    }
+                }
+                tc_commit(k_empty(s));
+                tc_commit(acc_full(ab));
+                ++it_k;
+                ++it_acc;
+            }
+            if (!ok) break;
+            tc_commit(q_empty(qb));
+            ++it_q;
+        }
+        tc_commit(done_bar);                       // every MMA issued has completed
+        wait_bar(done_bar, 0, timeout_ns, nullptr);  // before TMEM is released
+    } else if (warp >= 2) {
+        // ---------------- epilogue ----------------
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;          // key within the tile = TMEM lane
+        int it_acc = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            const IdxUnit U = get_unit(u);
+            for (int kt = U.kt0; kt < U.kt1; ++kt) {
+                const int ab = it_acc & 1;
+                ok = wait_bar(acc_full(ab), (it_acc >> 1) & 1, timeout_ns, s_abort);
+                if (!ok) break;
+                tc_fence_after();
+                const int s = kt * kIdxTileKeys + row;
+#pragma unroll 1
+                for (int qi = 0; qi < NQ; ++qi) {
+                    if (qi >= U.nq) break;     // warp-uniform
+                    uint32_t v0[32], v1[32];
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                           static_cast<uint32_t>(ab * C::BN + qi * kIdxHeads);
+                    tmem_ld32(taddr, v0);
+                    tmem_ld32(taddr + 32, v1);
+                    tmem_ld_wait();
+                    const float4* w4 = reinterpret_cast<const float4*>(w + static_cast<long long>(U.q_row0 + qi) * kIdxHeads);
+                    float acc = 0.f;
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 ww = __ldg(w4 + j4);
+                        acc = fmaf(ww.x, fmaxf(__uint_as_float(v0[4 * j4 + 0]), 0.f), acc);
+                        acc = fmaf(ww.y, fmaxf(__uint_as_float(v0[4 * j4 + 1]), 0.f), acc);
+                        acc = fmaf(ww.z, fmaxf(__uint_as_float(v0[4 * j4 + 2]), 0.f), acc);
+                        acc = fmaf(ww.w, fmaxf(__uint_as_float(v0[4 * j4 + 3]), 0.f), acc);
+                    }
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 ww = __ldg(w4 + 8 + j4);
+                        acc = fmaf(ww.x, fmaxf(__uint_as_float(v1[4 * j4 + 0]), 0.f), acc);
+                        acc = fmaf(ww.y, fmaxf(__uint_as_float(v1[4 * j4 + 1]), 0.f), acc);
+                        acc = fmaf(ww.z, fmaxf(__uint_as_float(v1[4 * j4 + 2]), 0.f), acc);
+                        acc = fmaf(ww.w, fmaxf(__uint_as_float(v1[4 * j4 + 3]), 0.f), acc);
+                    }
+                    if (s <= U.t0 + qi) scores[static_cast<long long>(U.q_row0 + qi) * ld + s] = acc;
+                }
+                tc_fence_before();
+                mbar_arrive(acc_empty(ab));
+                ++it_acc;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace dsa

@@ -5,8 +5,8 @@ arithmetic, so both the CUDA library's tests/benchmark and the CPU oracle
 can take their inputs from it.
 
 Recipe (all workloads): a ``torch.Generator`` seeded with ``seed`` on the
-target device draws, in this order, q_I, k_I, w, q, kv as float32 standard
-normals; q_I, k_I, q and kv are divided by sqrt(last dim) and w by
+target device draws (``Tensor.normal_``), in this order, q_I, k_I, w, q, kv
+as float32 standard normals; q_I, k_I, q and kv are divided by sqrt(last dim) and w by
 sqrt(H_I); bf16 workloads then round to bfloat16.  The long-prefill
 workload adds one scalar per key position, drawn from N(0, std 0.5), to
 every element of that position's indexer key (so that some keys score high
@@ -92,7 +92,7 @@ def _lengths(cfg: DSAConfig, seed: int):
 
 
 def _draw(g, shape, denom, device):
-    x = torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+    x = torch.empty(*shape, device=device, dtype=torch.float32).normal_(generator=g)
     x.div_(denom)
     return x
 
@@ -110,7 +110,7 @@ def make_prefill_inputs(cfg: DSAConfig, device="cpu", seed: int = 0):
     q = _draw(g, (T, cfg.n_heads, cfg.d_qk), math.sqrt(cfg.d_qk), device).to(dt)
     kv = _draw(g, (T, cfg.d_qk), math.sqrt(cfg.d_qk), device).to(dt)
     if cfg.key_offset_std > 0:
-        off = torch.randn(T, 1, generator=g, device=device, dtype=torch.float32) * cfg.key_offset_std
+        off = torch.empty(T, 1, device=device, dtype=torch.float32).normal_(generator=g) * cfg.key_offset_std
         k_idx.add_(off)
     cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
     cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)

@@ -1,0 +1,85 @@
+"""Comparison helpers shared by the GPU parity tests (no method arithmetic
+beyond the tolerance denominators the acceptance criteria define)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# Acceptance tolerances (bf16 inputs, fp32 accumulation on the GPU):
+SCORE_REL = 2e-3        # |dI| <= 2e-3 * max(|I|, A),  A = sum_j |w_j| ReLU(q_j . k)
+ATTN_MAX_ABS = 2e-2     # attention output, max abs error against the fp64 oracle
+ATTN_MEAN_ABS = 2e-3    # attention output, mean abs error
+LSE_ABS = 2e-3          # log-sum-exp (natural log)
+TIE_REL = 1e-5          # near-tie band of the k-th oracle score
+# fp32 inputs (general kernels, fp32 throughout): rounding ~1e-6 relative
+FP32_ATTN_MAX_ABS = 1e-4
+FP32_SCORE_REL = 1e-4
+
+
+def f64(x):
+    if isinstance(x, torch.Tensor):
+        return x.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def score_denominator(q_idx_t, w_t, k_prefix, full=False):
+    """A[s] = sum_j |w_j| * ReLU(q_j . k_s): the scale of the terms that add up to I[s].
+
+    full=True gives sum_j |w_j| * sum_d |q_jd k_sd| instead, the scale that
+    also covers cancellation inside each dot product (used for the tighter
+    fp32 check, where rounding of near-zero dots is visible)."""
+    if full:
+        dots = np.abs(f64(q_idx_t)) @ np.abs(f64(k_prefix)).T
+        return np.abs(f64(w_t)) @ dots
+    dots = f64(q_idx_t) @ f64(k_prefix).T
+    return np.abs(f64(w_t)) @ np.maximum(dots, 0.0)
+
+
+def check_scores(gpu_row, ref_row, denom, rel):
+    gpu_row = f64(gpu_row)
+    bound = rel * np.maximum(np.abs(ref_row), denom) + 1e-30
+    err = np.abs(gpu_row - ref_row)
+    bad = np.nonzero(err > bound)[0]
+    assert bad.size == 0, f"{bad.size} scores out of tolerance, e.g. s={bad[:5]} gpu={gpu_row[bad[:5]]} ref={ref_row[bad[:5]]}"
+
+
+def check_selection(gpu_idx, ref_scores, ref_idx, k):
+    """GPU selection = oracle selection, except elements tied with the k-th
+    oracle score within the near-tie band."""
+    g = np.asarray(gpu_idx, dtype=np.int64)
+    n = len(ref_scores)
+    keep = min(k, n)
+    assert np.all(g[keep:] == -1), "padding must be -1"
+    sel = g[:keep]
+    assert np.all(np.diff(sel) > 0), "selected positions must be strictly ascending"
+    assert sel.min() >= 0 and sel.max() < n
+    ref = np.asarray(ref_idx[:keep], dtype=np.int64)
+    if np.array_equal(sel, ref):
+        return 0
+    tau = np.sort(ref_scores)[::-1][keep - 1]
+    band = TIE_REL * abs(tau) + 1e-7 * np.max(np.abs(ref_scores))
+    diff = np.setxor1d(sel, ref)
+    far = diff[np.abs(ref_scores[diff] - tau) > band]
+    assert far.size == 0, f"selection differs away from the k-th score: {far[:8]} (tau={tau})"
+    return diff.size
+
+
+def check_attention(gpu_out, ref_out, max_abs=ATTN_MAX_ABS, mean_abs=ATTN_MEAN_ABS):
+    e = np.abs(f64(gpu_out) - ref_out)
+    assert e.max() <= max_abs, f"max abs err {e.max():.3e} > {max_abs}"
+    assert e.mean() <= mean_abs, f"mean abs err {e.mean():.3e} > {mean_abs}"
+    return float(e.max()), float(e.mean())
+
+
+def sample_rows(cu, k, per_seq=8, seed=0):
+    """Deterministic sample of packed rows: t in {0, k-2, k-1, k, L-1} plus random rows per sequence."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    cu = [int(c) for c in cu]
+    for b in range(len(cu) - 1):
+        lo, hi = cu[b], cu[b + 1]
+        L = hi - lo
+        pos = {0, k - 2, k - 1, k, L - 1}
+        pos |= set(int(x) for x in rng.integers(0, L, size=per_seq))
+        rows += [lo + t for t in sorted(pos) if 0 <= t < L]
+    return rows

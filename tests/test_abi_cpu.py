@@ -1,0 +1,113 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every function that include/dsa.h declares,
+and reject bad arguments on the host before anything touches a device.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from sparse_attention_long_gemm_b300 import _binding as B
+from sparse_attention_long_gemm_b300.build import build_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_library()
+    return B.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_and_library_exports_everything(L):
+    names = _declared()
+    assert "dsa_forward" in names and "dsa_forward_decode" in names
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (dsa_[a-z_]+)\b", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    assert set(B.EXPORTED) == set(names)
+    for n in names:
+        assert hasattr(L, n)
+
+
+V32 = dict(n_idx_heads=64, idx_dim=128, n_heads=128, d_qk=576, d_v=512, topk=2048, softmax_scale=0.07,
+           dtype="bf16")
+TINY = dict(n_idx_heads=4, idx_dim=32, n_heads=8, d_qk=80, d_v=64, topk=64, softmax_scale=0.1, dtype="fp32")
+
+
+def test_status_strings_and_path_names(L):
+    for code in range(0, -8, -1):
+        assert B.status_string(code).startswith("DSA_")
+    assert B.dsa_path_name(B.make_params(**V32)) == "tcgen05"
+    assert B.dsa_path_name(B.make_params(**TINY)) == "simt"
+    bad = B.make_params(**{**V32, "d_v": 1000})
+    assert B.dsa_path_name(bad) == "invalid"
+
+
+def test_workspace_sizes(L):
+    p = B.make_params(**V32)
+    ws = B.dsa_workspace_size(p, 4096, 4096, 1)
+    assert ws == 4096 * 4096 * 4 + 4096 * 2048 * 4
+    ws = B.dsa_workspace_size(p, 10, 7, 2)          # ld rounds 7 up to 8, each part to 256 B
+    assert ws == 512 + 81920
+    assert B.dsa_decode_workspace_size(p, 64, 65536) == 64 * 65536 * 4 + 64 * 2048 * 4
+    assert B.dsa_workspace_size(p, 10, 0, 1) == 0
+    assert B.dsa_decode_workspace_size(B.make_params(**{**V32, "topk": 0}), 4, 4) == 0
+
+
+def _fake(n=1 << 12):
+    """A 256-byte aligned host address: never dereferenced, validation fails first."""
+    return ctypes.c_void_p(0x10000)
+
+
+def test_host_validation_rejects_bad_arguments(L):
+    p = B.make_params(**V32)
+    P = ctypes.byref(p)
+    f = _fake()
+    null = None
+    s = None
+    # null params / pointers
+    assert L.dsa_index_scores(None, f, f, f, f, 1, 8, 8, f, 8, s) == B.DSA_ERR_ARG
+    assert L.dsa_index_scores(P, null, f, f, f, 1, 8, 8, f, 8, s) == B.DSA_ERR_ARG
+    assert L.dsa_topk(P, f, 8, null, 1, 8, 8, f, s) == B.DSA_ERR_ARG
+    # ld too small / not a multiple of 4
+    assert L.dsa_index_scores(P, f, f, f, f, 1, 8, 16, f, 8, s) == B.DSA_ERR_SHAPE
+    assert L.dsa_topk(P, f, 10, f, 1, 8, 8, f, s) == B.DSA_ERR_SHAPE
+    # misaligned pointer
+    assert L.dsa_sparse_mla_attn(P, ctypes.c_void_p(0x10004), f, f, f, 1, 8, 8, f, None, s) == B.DSA_ERR_ARG
+    # bad dtype / unsupported shapes
+    bad = B.make_params(**{**V32, "dtype": 7})
+    assert L.dsa_topk(ctypes.byref(bad), f, 8, f, 1, 8, 8, f, s) == B.DSA_ERR_ARG
+    big = B.make_params(**{**V32, "topk": 20000})
+    assert L.dsa_topk(ctypes.byref(big), f, 8, f, 1, 8, 8, f, s) == B.DSA_ERR_UNSUPPORTED
+    wide = B.make_params(**{**V32, "n_idx_heads": 129})
+    assert L.dsa_index_scores(ctypes.byref(wide), f, f, f, f, 1, 8, 8, f, 8, s) == B.DSA_ERR_UNSUPPORTED
+    assert L.dsa_topk(P, f, 8, f, 0, 8, 8, f, s) == B.DSA_ERR_ARG          # batch < 1
+    assert L.dsa_topk(P, f, 1 << 21, f, 1, 8, (1 << 20) + 1, f, s) == B.DSA_ERR_UNSUPPORTED
+    # fused calls: missing / small / misaligned workspace
+    assert L.dsa_forward(P, f, f, f, f, f, f, 1, 8, 8, f, None, None, None, 0, s) == B.DSA_ERR_WORKSPACE
+    assert L.dsa_forward(P, f, f, f, f, f, f, 1, 8, 8, f, None, None, f, 100, s) == B.DSA_ERR_WORKSPACE
+    need = B.dsa_workspace_size(p, 8, 8, 1)
+    assert L.dsa_forward(P, f, f, f, f, f, f, 1, 8, 8, f, None, None, ctypes.c_void_p(0x10010), need,
+                         s) == B.DSA_ERR_WORKSPACE
+    assert L.dsa_forward_decode(P, f, f, f, f, f, f, 2, 16, f, None, None, f, 10, s) == B.DSA_ERR_WORKSPACE
+    assert L.dsa_forward_decode(P, f, f, f, f, f, null, 2, 16, f, None, None, f, 1 << 20, s) == B.DSA_ERR_ARG
+    # empty batch is a no-op that touches nothing
+    assert L.dsa_topk(P, f, 8, f, 1, 0, 8, f, s) == B.DSA_OK
+
+
+def test_wait_timeout_setting_is_clamped_and_returns_previous(L):
+    old = B.dsa_set_wait_timeout_ns(5000)
+    assert B.dsa_set_wait_timeout_ns(1) == 5000
+    assert B.dsa_set_wait_timeout_ns(old) == 1000
