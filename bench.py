@@ -137,15 +137,9 @@ def _sample_rows(L, k, n_extra, seed):
 
 def _host_copy_for_oracle(inp, rows):
     """Host copies the oracle needs: whole k_I / kv, and only the sampled rows of the per-query tensors."""
-    import torch
-
-    T = inp["q"].shape[0]
     out = {"k_idx": inp["k_idx"].cpu(), "kv": inp["kv"].cpu(), "cu_seqlens": inp["cu_seqlens"].cpu()}
     for name in ("q_idx", "w", "q"):
-        src = inp[name]
-        full = torch.zeros((T,) + tuple(src.shape[1:]), dtype=src.dtype) if False else None
-        sub = src[rows].cpu()
-        out[name] = _RowView(sub, rows)
+        out[name] = _RowView(inp[name][rows].cpu(), rows)
     return out
 
 

@@ -1,0 +1,135 @@
+"""Parity at the full workload sizes, in the launch configuration the
+benchmark times (index scores -> top-k -> sparse attention through the C
+ABI), checked on a seeded sample of rows that the oracle computes one by
+one, plus properties that must hold on every row.
+
+Inputs are drawn on the GPU (seeded); the oracle receives host copies of
+exactly those input tensors.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.dsa_oracle as O
+import sparse_attention_long_gemm_b300 as dsa
+from sparse_attention_long_gemm_b300 import _binding as B
+from sparse_attention_long_gemm_b300.build import build_library
+from sparse_attention_long_gemm_b300.synth import CONFIGS, make_decode_inputs, make_prefill_inputs
+
+from _helpers import (LSE_ABS, SCORE_REL, check_attention, check_scores, check_selection, sample_rows,
+                      score_denominator)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    build_library()
+    B.lib()
+    yield
+    torch.cuda.empty_cache()
+
+
+def _valid_rows_property(idx, pos, k):
+    """Every row: ascending, distinct, in [0, t], exactly min(k, t+1) entries, -1 padded."""
+    n = torch.clamp(pos + 1, max=k)
+    ar = torch.arange(k, device=idx.device)[None, :]
+    valid = ar < n[:, None]
+    assert torch.all((idx >= 0) == valid), "wrong number of selected entries"
+    assert torch.all(idx[~valid] == -1)
+    assert torch.all(torch.where(valid, idx <= pos[:, None], True)), "selected position after the query"
+    d = idx[:, 1:] - idx[:, :-1]
+    assert torch.all(torch.where(valid[:, 1:], d > 0, True)), "not strictly ascending"
+
+
+def _run_prefill(cfg, per_seq):
+    inp = make_prefill_inputs(cfg, DEV, seed=0)
+    p = B.params_from_config(cfg)
+    lens = inp["lengths"]
+    T, Bn, maxL = sum(lens), len(lens), inp["max_seqlen"]
+    ld = (maxL + 3) // 4 * 4
+    scores = torch.empty((T, ld), dtype=torch.float32, device=DEV)
+    idx = torch.empty((T, cfg.topk), dtype=torch.int32, device=DEV)
+    out = torch.empty((T, cfg.n_heads, cfg.d_v), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((T, cfg.n_heads), dtype=torch.float32, device=DEV)
+    B.dsa_index_scores(p, inp["q_idx"], inp["w"], inp["k_idx"], inp["cu_seqlens"], Bn, T, maxL, scores, ld)
+    B.dsa_topk(p, scores, ld, inp["cu_seqlens"], Bn, T, maxL, idx)
+    B.dsa_sparse_mla_attn(p, inp["q"], inp["kv"], idx, inp["cu_seqlens"], Bn, T, maxL, out, lse)
+    torch.cuda.synchronize()
+    assert B.dsa_get_device_error() == B.DSA_OK
+
+    cu = inp["cu_seqlens"].cpu()
+    pos = torch.cat([torch.arange(L, device=DEV, dtype=torch.int64) for L in lens])
+    _valid_rows_property(idx, pos, cfg.topk)
+
+    rows = sample_rows(cu.numpy(), cfg.topk, per_seq=per_seq, seed=7)
+    host = {"k_idx": inp["k_idx"].cpu(), "kv": inp["kv"].cpu()}
+    sub = {n: inp[n][rows].cpu() for n in ("q_idx", "w", "q")}
+    sc = scores[rows].cpu().numpy()
+    ix = idx[rows].cpu().numpy()
+    o = out[rows].float().cpu().numpy()
+    ls = lse[rows].cpu().numpy()
+    cun = cu.numpy()
+    ndiff = 0
+    for i, r in enumerate(rows):
+        b = int(np.searchsorted(cun, r, side="right") - 1)
+        lo, hi = int(cun[b]), int(cun[b + 1])
+        t = r - lo
+        kseq = host["k_idx"][lo:hi]
+        ref_sc = O.index_scores_row(sub["q_idx"][i], sub["w"][i], kseq[: t + 1])
+        check_scores(sc[i, : t + 1], ref_sc, score_denominator(sub["q_idx"][i], sub["w"][i], kseq[: t + 1]),
+                     SCORE_REL)
+        # top-k bit-exact on the GPU's own score row
+        assert np.array_equal(ix[i], O.topk_select(sc[i, : t + 1], cfg.topk)), f"top-k not bit-exact at row {r}"
+        # end to end against the oracle's fp64 scores (near ties exempt)
+        ref_idx = O.topk_select(ref_sc, cfg.topk)
+        ndiff += check_selection(ix[i], ref_sc, ref_idx, cfg.topk) > 0
+        mask = O.additive_mask_row(ix[i], hi - lo)
+        ref_o, ref_l = O.masked_attention_row(sub["q"][i], host["kv"][lo:hi], mask, cfg.softmax_scale, cfg.d_v)
+        check_attention(o[i], ref_o)
+        assert np.abs(ls[i] - ref_l).max() <= LSE_ABS
+    return ndiff, len(rows)
+
+
+def test_long_prefill_32k_sampled():
+    ndiff, n = _run_prefill(CONFIGS["long"], per_seq=24)
+    assert ndiff <= n // 4
+
+
+def test_v32_prefill_4k_sampled():
+    _run_prefill(CONFIGS["v32"], per_seq=24)
+
+
+def test_varlen_packed_sampled():
+    _run_prefill(CONFIGS["varlen"], per_seq=4)
+
+
+def test_decode_64x64k_sampled():
+    cfg = CONFIGS["decode"]
+    inp = make_decode_inputs(cfg, DEV, seed=0)
+    p = B.params_from_config(cfg)
+    out, lse, idx = dsa.decode(p, inp["q_idx"], inp["w"], inp["q"], inp["idx_cache"], inp["kv_cache"],
+                               inp["cache_seqlens"], want_idx=True)
+    torch.cuda.synchronize()
+    assert B.dsa_get_device_error() == B.DSA_OK
+    lens = inp["lengths"]
+    _valid_rows_property(idx, inp["cache_seqlens"].long() - 1, cfg.topk)
+    rng = np.random.default_rng(3)
+    batches = sorted(set([int(np.argmax(lens)), int(np.argmin(lens))] + rng.integers(0, cfg.batch, 6).tolist()))
+    ix = idx.cpu().numpy()
+    o = out.float().cpu().numpy()
+    ls = lse.cpu().numpy()
+    for b in batches:
+        n = lens[b]
+        kc = inp["idx_cache"][b, :n].cpu()
+        vc = inp["kv_cache"][b, :n].cpu()
+        ref_sc = O.index_scores_row(inp["q_idx"][b].cpu(), inp["w"][b].cpu(), kc)
+        ref_idx = O.topk_select(ref_sc, cfg.topk)
+        check_selection(ix[b], ref_sc, ref_idx, cfg.topk)
+        mask = O.additive_mask_row(ix[b], n)
+        ref_o, ref_l = O.masked_attention_row(inp["q"][b].cpu(), vc, mask, cfg.softmax_scale, cfg.d_v)
+        check_attention(o[b], ref_o)
+        assert np.abs(ls[b] - ref_l).max() <= LSE_ABS
