@@ -191,6 +191,40 @@ int dsa_selftest_wait_timeout(long long timeout_ns, void* stream);
  * "tcgen05" (sm_103a tensor-core kernels) or "simt" (general kernels). */
 const char* dsa_path_name(const dsa_params* params);
 
+/* Decode forward for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart: this is a library convenience.  Some
+ * callers have no way to obtain a workspace: plug-in code that runs inside
+ * another framework without access to its allocator, or a serving loop
+ * whose device memory is entirely owned by a pool it does not control and
+ * which cannot afford the device-wide synchronisation a cudaMalloc may
+ * cause in the middle of a step.  This entry point computes exactly what
+ * dsa_forward_decode computes, with the same kernels and arguments, but
+ * keeps its scratch (score rows and, when idx_out is NULL, the selected
+ * indices) in one array of DSA_NOALLOC_SCRATCH_BYTES that the library
+ * reserves statically on every GPU that loads it, for the life of the
+ * process.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   Limits: batch * round_up(max_ctx, 4) <= DSA_NOALLOC_MAX_SCORES floats and,
+ *   when idx_out is NULL, batch * topk <= DSA_NOALLOC_MAX_INDICES ints;
+ *   larger problems return DSA_ERR_UNSUPPORTED before anything is enqueued.
+ *   Set-up: the first call on a device (with that device current) looks up
+ *   the array's device address; make that first call before any stream
+ *   capture begins.
+ *   Sharing: every call on a device uses the same array and leaves the last
+ *   call's contents in it; nothing in it has to start at zero (each call
+ *   writes every entry it later reads).  Calls whose GPU work overlaps in
+ *   time (different streams, or different host threads) race on the array:
+ *   serialise them, for instance on one stream.
+ *   Arguments, layouts and the other errors are those of dsa_forward_decode. */
+#define DSA_NOALLOC_MAX_SCORES  (4u << 20)    /* 4 Mi floats: 16 MiB of score rows */
+#define DSA_NOALLOC_MAX_INDICES (128u << 10)  /* 128 Ki ints: 512 KiB of indices   */
+#define DSA_NOALLOC_SCRATCH_BYTES (4u * DSA_NOALLOC_MAX_SCORES + 4u * DSA_NOALLOC_MAX_INDICES)
+int dsa_forward_decode_noalloc(const dsa_params* params, const void* q_idx, const float* w,
+                               const void* q, const void* idx_cache, const void* kv_cache,
+                               const int* cache_seqlens, int batch, int max_ctx,
+                               void* out, float* lse, int* idx_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,6 +23,8 @@ DSA_ERR_WORKSPACE = -6
 DSA_ERR_DEVICE_DATA = -7
 DSA_BF16 = 0
 DSA_FP32 = 1
+DSA_NOALLOC_MAX_SCORES = 4 << 20
+DSA_NOALLOC_MAX_INDICES = 128 << 10
 
 EXPORTED = [
     "dsa_status_string",
@@ -37,6 +39,7 @@ EXPORTED = [
     "dsa_set_wait_timeout_ns",
     "dsa_selftest_wait_timeout",
     "dsa_path_name",
+    "dsa_forward_decode_noalloc",
 ]
 
 
@@ -91,6 +94,8 @@ def lib():
         L.dsa_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, i, i, i, vp, vp, vp, vp, sz, vp]
         L.dsa_forward_decode.restype = i
         L.dsa_forward_decode.argtypes = [P, vp, vp, vp, vp, vp, vp, i, i, vp, vp, vp, vp, sz, vp]
+        L.dsa_forward_decode_noalloc.restype = i
+        L.dsa_forward_decode_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, i, i, vp, vp, vp, vp]
         L.dsa_get_device_error.restype = i
         L.dsa_get_device_error.argtypes = [vp]
         L.dsa_set_wait_timeout_ns.restype = ll
@@ -181,6 +186,15 @@ def dsa_forward_decode(p, q_idx, w, q, idx_cache, kv_cache, cache_seqlens, batch
                                   _ptr(idx_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _stream(stream))
     _check(rc, "dsa_forward_decode")
+
+
+def dsa_forward_decode_noalloc(p, q_idx, w, q, idx_cache, kv_cache, cache_seqlens, batch, max_ctx, out, lse,
+                               idx_out, stream=None):
+    """Decode forward with the library's own fixed-size scratch (no workspace argument)."""
+    rc = lib().dsa_forward_decode_noalloc(ctypes.byref(p), _ptr(q_idx), _ptr(w), _ptr(q), _ptr(idx_cache),
+                                          _ptr(kv_cache), _ptr(cache_seqlens), batch, max_ctx, _ptr(out),
+                                          _ptr(lse), _ptr(idx_out), _stream(stream))
+    _check(rc, "dsa_forward_decode_noalloc")
 
 
 def dsa_get_device_error(stream=None) -> int:

@@ -374,3 +374,66 @@ extern "C" int dsa_selftest_wait_timeout(long long timeout_ns, void* stream) {
         static_cast<unsigned long long>(timeout_ns));
     return launch_status();
 }
+
+// ---------------------------------------------------------------------------
+// dsa_forward_decode_noalloc: decode forward with library-owned scratch.
+//
+// For callers that cannot allocate device memory (see include/dsa.h).  The
+// scratch is one statically reserved array per device; host code must not
+// pass the array's name to a kernel (in host code it only stands for the
+// symbol), so its device address is looked up once per device with
+// cudaGetSymbolAddress and cached.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up on
+// the first call for that device).
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return DSA_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" int dsa_forward_decode_noalloc(const dsa_params* params, const void* q_idx, const float* w,
+                                          const void* q, const void* idx_cache, const void* kv_cache,
+                                          const int* cache_seqlens, int batch, int max_ctx, void* out,
+                                          float* lse, int* idx_out, void* stream) {
+    int rc = check_params(params);
+    if (rc != DSA_OK) return rc;
+    if (q_idx == nullptr || w == nullptr || q == nullptr || idx_cache == nullptr || kv_cache == nullptr ||
+        cache_seqlens == nullptr || out == nullptr || batch < 1 || max_ctx < 1)
+        return DSA_ERR_ARG;
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(q) || !aligned16(idx_cache) || !aligned16(kv_cache) ||
+        !aligned16(out) || (lse && !aligned16(lse)) || (idx_out && !aligned16(idx_out)))
+        return DSA_ERR_ARG;
+    const long long ld = round_up(max_ctx, 4);
+    if (static_cast<long long>(batch) * ld > static_cast<long long>(DSA_NOALLOC_MAX_SCORES)) return DSA_ERR_UNSUPPORTED;
+    if (idx_out == nullptr &&
+        static_cast<long long>(batch) * params->topk > static_cast<long long>(DSA_NOALLOC_MAX_INDICES))
+        return DSA_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch)) != DSA_OK) return rc;
+    float* scores = static_cast<float*>(scratch);
+    int* idx = idx_out ? idx_out
+                       : reinterpret_cast<int*>(static_cast<char*>(scratch) + 4ull * DSA_NOALLOC_MAX_SCORES);
+    const RowSpec rs{cache_seqlens, batch, 1, max_ctx};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long key_rows = static_cast<long long>(batch) * max_ctx;
+    if ((rc = run_index_scores(params, q_idx, w, idx_cache, rs, batch, key_rows, scores, ld, st)) != DSA_OK) return rc;
+    if ((rc = run_topk(params, scores, ld, rs, batch, idx, st)) != DSA_OK) return rc;
+    return run_attn(params, q, kv_cache, idx, rs, batch, out, lse, st);
+}
