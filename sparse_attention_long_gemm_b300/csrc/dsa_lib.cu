@@ -8,6 +8,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -106,17 +107,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D bf16 tensor [rows, cols] (row stride = cols elements), box [box_rows, 64]
-// with 128-byte swizzle: each box row is one 128-byte swizzle row.
-int make_tmap_bf16(CUtensorMap* tm, const void* base, long long rows, long long cols, int box_rows) {
+// 2-D bf16 tensor [rows, cols] (row stride = cols elements), box
+// [box_rows, box_cols] with the given swizzle (box_cols * 2 bytes must not
+// exceed the swizzle span).
+int make_tmap_bf16(CUtensorMap* tm, const void* base, long long rows, long long cols, int box_rows, int box_cols = 64,
+                   CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (fn == nullptr) return DSA_ERR_CUDA;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_CUDA;
 }
@@ -168,18 +171,24 @@ int run_topk(const dsa_params* p, const float* scores, long long ld, const RowSp
 }
 
 int run_attn(const dsa_params* p, const void* q, const void* kv, const int* idx, const RowSpec& rs, int rows,
-             void* out, float* lse, cudaStream_t st) {
+             long long key_rows, void* out, float* lse, cudaStream_t st) {
     DevInfo* di = nullptr;
     int rc = device_info(&di);
     if (rc != DSA_OK) return rc;
     if (is_tc_shape(p)) {
-        CUtensorMap tq;
-        if ((rc = make_tmap_bf16(&tq, q, static_cast<long long>(rows) * kAttnHeads, kAttnDqk, kAttnHeads)) != DSA_OK)
+        CUtensorMap tq, tqr, tkv, tkvr;
+        const long long qrows = static_cast<long long>(rows) * kAttnHeads;
+        if ((rc = make_tmap_bf16(&tq, q, qrows, kAttnDqk, kAttnHeads)) != DSA_OK) return rc;
+        if ((rc = make_tmap_bf16(&tqr, q, qrows, kAttnDqk, kAttnHeads, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != DSA_OK)
+            return rc;
+        if ((rc = make_tmap_bf16(&tkv, kv, key_rows, kAttnDqk, 1)) != DSA_OK) return rc;
+        if ((rc = make_tmap_bf16(&tkvr, kv, key_rows, kAttnDqk, 1, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != DSA_OK)
             return rc;
         const float scale_log2 = p->softmax_scale * 1.4426950408889634f;
-        attn_tc_kernel<<<2 * rows, kAttnThreads, AttnTc::SMEM, st>>>(
-            tq, static_cast<const __nv_bfloat16*>(kv), idx, rs, p->topk, scale_log2,
-            static_cast<__nv_bfloat16*>(out), lse, static_cast<unsigned long long>(g_timeout_ns.load()));
+        const int nclusters = std::max(1, std::min(rows, di->sm_count / 2));
+        attn_tc_kernel<<<2 * nclusters, kAttnThreads, AttnTc::SMEM, st>>>(
+            tq, tqr, tkv, tkvr, idx, rs, rows, p->topk, scale_log2, static_cast<__nv_bfloat16*>(out), lse,
+            static_cast<unsigned long long>(g_timeout_ns.load()));
         return launch_status();
     }
     const dim3 grid(rows, p->n_heads);
@@ -279,7 +288,7 @@ int dsa_sparse_mla_attn(const dsa_params* params, const void* q, const void* kv,
         return DSA_ERR_ARG;
     if (total_q == 0) return DSA_OK;
     const RowSpec rs{cu_seqlens, batch, 0, max_seqlen};
-    return run_attn(params, q, kv, idx, rs, total_q, out, lse, static_cast<cudaStream_t>(stream));
+    return run_attn(params, q, kv, idx, rs, total_q, total_q, out, lse, static_cast<cudaStream_t>(stream));
 }
 
 int dsa_forward(const dsa_params* params, const void* q_idx, const float* w, const void* k_idx, const void* q,
@@ -305,7 +314,7 @@ int dsa_forward(const dsa_params* params, const void* q_idx, const float* w, con
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((rc = run_index_scores(params, q_idx, w, k_idx, rs, total_q, total_q, scores, ld, st)) != DSA_OK) return rc;
     if ((rc = run_topk(params, scores, ld, rs, total_q, idx, st)) != DSA_OK) return rc;
-    return run_attn(params, q, kv, idx, rs, total_q, out, lse, st);
+    return run_attn(params, q, kv, idx, rs, total_q, total_q, out, lse, st);
 }
 
 int dsa_forward_decode(const dsa_params* params, const void* q_idx, const float* w, const void* q,
@@ -334,7 +343,7 @@ int dsa_forward_decode(const dsa_params* params, const void* q_idx, const float*
     const long long key_rows = static_cast<long long>(batch) * max_ctx;
     if ((rc = run_index_scores(params, q_idx, w, idx_cache, rs, batch, key_rows, scores, ld, st)) != DSA_OK) return rc;
     if ((rc = run_topk(params, scores, ld, rs, batch, idx, st)) != DSA_OK) return rc;
-    return run_attn(params, q, kv_cache, idx, rs, batch, out, lse, st);
+    return run_attn(params, q, kv_cache, idx, rs, batch, key_rows, out, lse, st);
 }
 
 int dsa_get_device_error(void* stream) {
@@ -435,5 +444,5 @@ extern "C" int dsa_forward_decode_noalloc(const dsa_params* params, const void* 
     const long long key_rows = static_cast<long long>(batch) * max_ctx;
     if ((rc = run_index_scores(params, q_idx, w, idx_cache, rs, batch, key_rows, scores, ld, st)) != DSA_OK) return rc;
     if ((rc = run_topk(params, scores, ld, rs, batch, idx, st)) != DSA_OK) return rc;
-    return run_attn(params, q, kv_cache, idx, rs, batch, out, lse, st);
+    return run_attn(params, q, kv_cache, idx, rs, batch, key_rows, out, lse, st);
 }
