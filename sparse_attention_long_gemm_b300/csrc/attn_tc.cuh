@@ -122,6 +122,14 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int 
         : "memory");
 }
 
+// Asynchronous store of 16 bytes into another CTA's shared memory (address
+// from mapa); completes `bytes` on that CTA's mbarrier (also from mapa).
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(raddr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar) : "memory");
+}
+
 // Rows of one query: number of valid selected entries and of 64-key blocks.
 struct AttnRow {
     RowInfo ri;
@@ -174,8 +182,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(q_stage_free, 128);
         for (int i = 0; i < kAttnStages; ++i) { mbar_init(kv_full(i), 1); mbar_init(kv_empty(i), 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(s_full(i), 1); mbar_init(p_full(i), 128); mbar_init(pv_done(i), 1); }
-        mbar_init(x_full, 128);
-        mbar_init(x_free, 128);
+        mbar_init(x_full, 1);       // the local expect_tx; the peer's bytes complete it
+        mbar_init(x_free, 4);       // one arrive per softmax warp of the peer
         mbar_init(done_bar, 1);
         *s_abort = 0;
         fence_mbar_init();
@@ -216,20 +224,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (!ok) break;
             const int* irow = idx + static_cast<long long>(r) * k;
             const int kb = static_cast<int>(A.ri.key_base);
+            // this lane's 4 entries of block i (lanes 0..15 cover the 64 keys); loads run
+            // three blocks ahead of their use so their latency hides behind the ring
+            auto load_ent = [&](int i, int (&v)[4]) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int ent = i * kAttnBK + 4 * (lane & 15) + e;
+                    v[e] = (ent < A.nsel) ? __ldg(irow + ent) : 0;
+                }
+            };
+            int e0[4], e1[4], e2[4];
+            load_ent(0, e0);
+            load_ent(1, e1);
+            load_ent(2, e2);
             for (int i = 0; i < A.nb && ok; ++i, ++gi) {
                 const int st = gi % kAttnStages;
-                // this lane's 4 rows (lanes 0..15 cover the 64 keys of the block)
                 int rw[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int ent = i * kAttnBK + 4 * (lane & 15) + e;
-                    int s = (ent < A.nsel) ? __ldg(irow + ent) : 0;
+                    int s = e0[e];
                     if (s < 0 || s >= A.ri.n) {
                         if (ent < A.nsel) raise_error(DSA_ERR_DEVICE_DATA);
                         s = 0;   // any in-range row; entries past nsel are masked by the softmax
                     }
                     rw[e] = kb + s;
+                    e0[e] = e1[e];
+                    e1[e] = e2[e];
                 }
+                load_ent(i + 3, e2);
                 if (lane == 0) {
                     ok = wait_bar(kv_empty(st), ((gi / kAttnStages) & 1) ^ 1, timeout_ns, s_abort);
                     if (ok) mbar_expect_tx(kv_full(st), C::KV_TX);
@@ -255,26 +278,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (lane == 0) {
             int qi = 0, gi = 0;
             bool ok = true;
+            // descriptors of stage 0 / rope buffer 0; other stages and K-steps are offsets
+            // of the start-address field (16-byte units)
+            const uint64_t dK0 = sdesc_sw128(sKV, 16, 1024);              // keys, latent slots (K-major)
+            const uint64_t dR0 = sdesc_sw64(sKV + 4 * C::KV_SLOT);        // keys, rope part
+            const uint64_t dV0 = sdesc_sw128(sKV, C::KV_SLOT, 1024);      // values (MN-major)
+            const uint64_t dQR0 = sdesc_sw64(sQR);                        // Q rope part
             auto issue_qk = [&](int g, int qb) -> bool {
                 const int st = g % kAttnStages;
                 if (!wait_bar(kv_full(st), (g / kAttnStages) & 1, timeout_ns, s_abort)) return false;
                 tc_fence_after();
                 const uint32_t d = tmem_base + C::TM_SP + (g & 1) * kAttnBK;
-                const uint32_t stage = sKV + st * C::KV_STAGE;
+                const uint64_t so = static_cast<uint64_t>((st * C::KV_STAGE) >> 4);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t b = sdesc_sw128(stage + j * C::KV_SLOT + kk * 32, 16, 1024);
-                        tc_mma_bf16_ts(d, tmem_base + C::TM_Q + j * 32 + kk * 8, b, C::IDESC_QK, (j | kk) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_bf16_ts(d, tmem_base + C::TM_Q + j * 32 + kk * 8,
+                                       dK0 + so + static_cast<uint64_t>((j * C::KV_SLOT + kk * 32) >> 4), C::IDESC_QK,
+                                       (j | kk) ? 1u : 0u);
                 }
+                const uint64_t qo = static_cast<uint64_t>((qb * C::QR_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const uint64_t a = sdesc_sw64(sQR + qb * C::QR_BYTES + kk * 32);
-                    const uint64_t b = sdesc_sw64(stage + 4 * C::KV_SLOT + kk * 32);
-                    tc_mma_bf16(d, a, b, C::IDESC_QK, 1u);
-                }
+                for (int kk = 0; kk < 2; ++kk)
+                    tc_mma_bf16(d, dQR0 + qo + static_cast<uint64_t>(kk * 2), dR0 + so + static_cast<uint64_t>(kk * 2),
+                                C::IDESC_QK, 1u);
                 tc_commit(s_full(g & 1));
                 return true;
             };
@@ -295,14 +323,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     if (!ok) break;
                     tc_fence_after();
                     const int st = g % kAttnStages;
-                    const uint32_t stage = sKV + st * C::KV_STAGE;
+                    const uint64_t so = static_cast<uint64_t>((st * C::KV_STAGE) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kAttnBK / 16; ++kk) {
+                    for (int kk = 0; kk < kAttnBK / 16; ++kk)
                         // V (MN-major): the 4 latent slots are the 64-column chunks (LBO), 8-key groups 1 KB apart
-                        const uint64_t b = sdesc_sw128(stage + kk * 16 * 128, C::KV_SLOT, 1024);
-                        tc_mma_bf16_ts(tmem_base + C::TM_O, tmem_base + C::TM_SP + (g & 1) * kAttnBK + kk * 8, b,
-                                       C::IDESC_PV, (i | kk) ? 1u : 0u);
-                    }
+                        tc_mma_bf16_ts(tmem_base + C::TM_O, tmem_base + C::TM_SP + (g & 1) * kAttnBK + kk * 8,
+                                       dV0 + so + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::IDESC_PV,
+                                       (i | kk) ? 1u : 0u);
                     tc_commit(pv_done(g & 1));
                     tc_commit(kv_empty(st));
                     if (i + 2 < A.nb) ok = issue_qk(g + 2, qb);
@@ -372,15 +399,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tmem_ld32(tmem_base + lane_off + C::TM_SP + b * kAttnBK + 32,
                           *reinterpret_cast<uint32_t(*)[32]>(sraw + 32));
                 tmem_ld_wait();
-                // exchange the partial scores with the peer CTA
+                // exchange the partial scores with the peer CTA: asynchronous remote stores
+                // that complete the peer's x_full transaction count
                 ok = __all_sync(0xffffffffu, wait_bar<true>(x_free, (g & 1) ^ 1, timeout_ns, s_abort));
                 if (!ok) break;
 #pragma unroll
                 for (int c = 0; c < 16; ++c)
-                    st_cluster_v4(sX_peer + h * 256 + (((c ^ h) & 15) << 4), __uint_as_float(sraw[4 * c]),
-                                  __uint_as_float(sraw[4 * c + 1]), __uint_as_float(sraw[4 * c + 2]),
-                                  __uint_as_float(sraw[4 * c + 3]));
-                mbar_arrive_cluster(x_full_peer);
+                    st_async_v4(sX_peer + h * 256 + (((c ^ h) & 15) << 4), sraw[4 * c], sraw[4 * c + 1], sraw[4 * c + 2],
+                                sraw[4 * c + 3], x_full_peer);
+                if (h == 0) mbar_expect_tx(x_full, C::X_BYTES);
                 ok = __all_sync(0xffffffffu, wait_bar<true>(x_full, g & 1, timeout_ns, s_abort));
                 if (!ok) break;
                 float sv[64];
@@ -392,7 +419,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     sv[4 * c + 2] = __uint_as_float(sraw[4 * c + 2]) + v.z;
                     sv[4 * c + 3] = __uint_as_float(sraw[4 * c + 3]) + v.w;
                 }
-                mbar_arrive_cluster(x_free_peer);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(x_free_peer);   // this warp's rows of X may be overwritten
                 // columns past the last valid entry are masked (identical for every head)
                 const int nvalid = A.nsel - i * kAttnBK;
                 float mx = -INFINITY;
