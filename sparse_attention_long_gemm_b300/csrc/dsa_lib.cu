@@ -176,19 +176,16 @@ int run_attn(const dsa_params* p, const void* q, const void* kv, const int* idx,
     int rc = device_info(&di);
     if (rc != DSA_OK) return rc;
     if (is_tc_shape(p)) {
-        CUtensorMap tq, tqr, tkv, tkvr;
+        CUtensorMap tq, tqr;
         const long long qrows = static_cast<long long>(rows) * kAttnHeads;
         if ((rc = make_tmap_bf16(&tq, q, qrows, kAttnDqk, kAttnHeads)) != DSA_OK) return rc;
-        if ((rc = make_tmap_bf16(&tqr, q, qrows, kAttnDqk, kAttnHeads, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != DSA_OK)
-            return rc;
-        if ((rc = make_tmap_bf16(&tkv, kv, key_rows, kAttnDqk, 1)) != DSA_OK) return rc;
-        if ((rc = make_tmap_bf16(&tkvr, kv, key_rows, kAttnDqk, 1, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != DSA_OK)
-            return rc;
+        if ((rc = make_tmap_bf16(&tqr, q, qrows, kAttnDqk, 64, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != DSA_OK) return rc;
+        (void)key_rows;
         const float scale_log2 = p->softmax_scale * 1.4426950408889634f;
         const int nclusters = std::max(1, std::min(rows, di->sm_count / 2));
         attn_tc_kernel<<<2 * nclusters, kAttnThreads, AttnTc::SMEM, st>>>(
-            tq, tqr, tkv, tkvr, idx, rs, rows, p->topk, scale_log2, static_cast<__nv_bfloat16*>(out), lse,
-            static_cast<unsigned long long>(g_timeout_ns.load()));
+            tq, tqr, static_cast<const __nv_bfloat16*>(kv), idx, rs, rows, p->topk, scale_log2,
+            static_cast<__nv_bfloat16*>(out), lse, static_cast<unsigned long long>(g_timeout_ns.load()));
         return launch_status();
     }
     const dim3 grid(rows, p->n_heads);
