@@ -13,20 +13,25 @@
 //   rank r owns latent columns 256r .. 256r+255 and rope columns
 //   512+32r .. 512+32r+31 (288 of the 576 contraction columns each).
 // Each rank gathers only its columns of the selected rows (no byte of a row
-// is fetched twice), computes a PARTIAL score tile S_r = Q_r . K_r^T over its
-// columns, and the two partials are exchanged through distributed shared
-// memory so both hold S = S_0 + S_1 (fp32 addition commutes, so both hold
-// bit-identical S and take identical softmax decisions).  Each rank then
-// accumulates O[:, its 256 latent columns] += P . V_r, where V_r is the
-// latent part of the columns it gathered.  No flop is duplicated.
+// is fetched twice) and computes PARTIAL scores S_r = Q_r . K_r^T for all 128
+// heads over its columns.  The softmax of a head is owned by one rank: rank r
+// owns heads 64r .. 64r+63.  Per 64-key block each rank sends the peer its
+// partial scores of the peer's heads (16 KB, fp32) and receives the peer's
+// partial scores of its own heads; it completes S = S_0 + S_1 for its heads,
+// runs their online softmax, and sends the peer their probabilities P (bf16)
+// together with each head's O rescale factor (and, for the final block, the
+// softmax denominators).  Both ranks then hold P for all 128 heads and
+// accumulate O[:, their 256 latent columns] += P . V_r.  No flop is
+// duplicated, and 24.5 KB per block cross between the CTAs in each
+// direction (distributed shared memory moves ~14.5 B/clk per SM, so these
+// bytes, not the tensor cores, would otherwise set the pace).
 //
 // Tensor memory of a CTA (512 columns x 128 lanes, lane = head):
 //   [0, 256)    O_r, fp32 accumulator
 //   [256, 384)  Q_r latent part, bf16 pairs: the A operand of Q.K^T
-//   [384, 448)  S/P buffer 0: fp32 partial scores of a 64-key block, then
-//               (after the exchange) the bf16 probabilities P over its first
-//               32 columns, which are the A operand of P.V
-//   [448, 512)  S/P buffer 1
+//   [384, 448)  S: fp32 partial scores of the current 64-key block (single:
+//               the next Q.K^T starts as soon as every lane has read it)
+//   [448, 512)  P buffers 0 and 1: bf16 probabilities, the A operand of P.V
 //
 // Shared memory is mostly a 4-slot ring.  Its items, in the order every role
 // walks them: per query, one Q item (two slots: the latent part of Q_r in
@@ -36,28 +41,29 @@
 // 64B-swizzled).  The softmax warps move a Q item into tensor memory (latent)
 // and a small rope buffer, freeing its slots at once, so nearly the whole ring
 // holds gathers in flight: random rows reach about 9 TB/s from L2 only with
-// ~100 KB per SM in flight and with requests of 512 contiguous bytes.
+// ~100 KB per SM in flight and with requests of 512 contiguous bytes.  The
+// rest holds the exchange buffers (received tiles double-buffered, outgoing
+// tiles staged once and sent by one bulk copy each).
 //
 // Per CTA (224 threads):
-//   warps 0..3  softmax: one head (TMEM lane) per thread; Q items into
-//               tensor memory, the score exchange (each thread stores its
-//               row of partial scores locally, then one bulk copy moves the
-//               32 KB tile into the peer CTA and completes the peer's
-//               mbarrier: single 16-byte remote stores reach only ~7 B/clk),
-//               the online softmax
-//               with a lazily updated running max (O is rescaled only when the
-//               max grows by more than 2^8), P into tensor memory, and the
-//               output epilogue;
-//   warp 4      TMEM allocation and tcgen05.mma issue (one thread);
+//   warps 0..3  softmax group, one head (TMEM lane) per thread.  The two
+//               warps whose lanes are this rank's heads ("own" warps)
+//               complete their scores, run the online softmax (running max
+//               updated lazily: O is rescaled only when it grows by more than
+//               2^8) and send P; the two others ("peer" warps) send their
+//               lanes' partial scores and move the P received for those
+//               heads into tensor memory, rescaling those O rows first when
+//               told to.  All four move Q items into tensor memory and run
+//               the output epilogue;
+//   warp 4      TMEM allocation and tcgen05.mma issue (one thread, polling
+//               both the next Q.K^T and the next P.V so neither waits on the
+//               other);
 //   warps 5..6  producers: the rows of a KV item by cp.async, each warp
 //               instruction one key's 512 latent bytes (the rope parts of 8
 //               keys per instruction), completion signalled with
 //               cp.async.mbarrier.arrive.noinc so the producers never wait for
 //               data; index loads run four blocks ahead; one thread issues the
 //               TMA loads of Q items.
-// MMA order per query: QK(0), QK(1), PV(0), QK(2), PV(1), QK(3), ...; a
-// QK(i+2) reuses the S/P buffer of PV(i), which is safe because tcgen05
-// operations issued by one thread execute in order.
 #pragma once
 
 #include <cuda.h>
@@ -81,26 +87,33 @@ struct AttnTc {
     static constexpr int QL_TILE = kAttnHeads * 128;                // 128 heads x 64 latent cols = 16 KB
     static constexpr int QR_HALF = 64 * 64;                         // 64 heads x 32 rope cols = 4 KB
     static constexpr int QR_BYTES = 2 * QR_HALF;
-    static constexpr int X_BYTES = kAttnHeads * kAttnBK * 4;        // peer's partial scores, 32 KB
+    static constexpr int XB = 64 * kAttnBK * 4;                     // partial scores of 64 heads: 16 KB
+    static constexpr int PB_P = 64 * kAttnBK * 2;                   // P of 64 heads: 8 KB
+    static constexpr int PB = PB_P + 64 * 4 + 64 * 4;               // + rescale factors + denominators
     static constexpr int OFF_RING = 0;
     static constexpr int OFF_QR = OFF_RING + kAttnSlots * SLOT;
-    static constexpr int OFF_X = OFF_QR + QR_BYTES;                 // the peer's partial scores land here
-    static constexpr int OFF_XS = OFF_X + X_BYTES;                  // this CTA's partial scores, sent in bulk
-    static constexpr int OFF_BAR = OFF_XS + X_BYTES;
-    // full[S], empty[S], q_tm_full, s_full[2], p_full[2], pv_done[2], x_full, x_free, done
-    static constexpr int NBAR = 2 * kAttnSlots + 1 + 2 + 2 + 2 + 3;
+    static constexpr int OFF_XR = OFF_QR + QR_BYTES;                // [2] received partial scores
+    static constexpr int OFF_XS = OFF_XR + 2 * XB;                  // outgoing partial scores
+    static constexpr int OFF_PR = OFF_XS + XB;                      // [2] received P message
+    static constexpr int OFF_PS = OFF_PR + 2 * PB;                  // outgoing P message
+    static constexpr int OFF_BAR = OFF_PS + PB;
+    // full[S], empty[S], q_tm_full, s_full, s_free, p_full[2], pv_done[2],
+    // xr_full[2], xr_free[2], pr_full[2], pr_free[2], done
+    static constexpr int NBAR = 2 * kAttnSlots + 1 + 1 + 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;               // + alignment slack
     static constexpr int TMEM_COLS = 512;
     static constexpr int TM_O = 0;
     static constexpr int TM_Q = 256;
-    static constexpr int TM_SP = 384;     // + 64 * buffer
+    static constexpr int TM_S = 384;
+    static constexpr int TM_P = 448;      // + 32 * buffer
     static constexpr uint32_t IDESC_QK = idesc_bf16(128, kAttnBK, false, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
     static constexpr uint32_t Q_TX = 4 * QL_TILE + QR_BYTES;
 };
 static_assert(AttnTc::SMEM <= 232448, "attention shared memory exceeds the per-CTA limit");
 static_assert(2 * AttnTc::QL_TILE + AttnTc::QR_HALF <= AttnTc::SLOT, "a Q item must fit in two slots");
+static_assert(AttnTc::PB % 16 == 0 && AttnTc::XB % 16 == 0, "bulk copies move multiples of 16 bytes");
 
 // Shared-memory matrix descriptor, 64-byte-swizzled K-major operand
 // (rows of 64 B, 8-row atoms of 512 B).
@@ -127,10 +140,14 @@ __device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
 
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into
 // another CTA's (address from mapa); completes `bytes` on that CTA's mbarrier.
+// Tracked in this thread's bulk async-group for bulk_wait_read().
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t rdst, uint32_t src, uint32_t bytes, uint32_t rbar) {
     asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(rdst), "r"(src), "r"(bytes), "r"(rbar) : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
+// Waits until every bulk copy committed by this thread has finished reading its source.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // Arrive on `bar` once every cp.async issued so far by this thread has landed
 // (the arrival counts against the barrier's expected count).
@@ -161,17 +178,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sRing = sbase + C::OFF_RING, sQR = sbase + C::OFF_QR, sX = sbase + C::OFF_X;
+    const uint32_t sRing = sbase + C::OFF_RING, sQR = sbase + C::OFF_QR;
     const uint32_t bar0 = sbase + C::OFF_BAR;
     auto full = [&](int i) { return bar0 + 8u * i; };
     auto empty = [&](int i) { return bar0 + 8u * (kAttnSlots + i); };
     const uint32_t q_tm_full = bar0 + 8u * (2 * kAttnSlots);
-    auto s_full = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 1 + i); };
+    const uint32_t s_full = bar0 + 8u * (2 * kAttnSlots + 1);
+    const uint32_t s_free = bar0 + 8u * (2 * kAttnSlots + 2);
     auto p_full = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 3 + i); };
     auto pv_done = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 5 + i); };
-    const uint32_t x_full = bar0 + 8u * (2 * kAttnSlots + 7);
-    const uint32_t x_free = bar0 + 8u * (2 * kAttnSlots + 8);
-    const uint32_t done_bar = bar0 + 8u * (2 * kAttnSlots + 9);
+    auto xr_full = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 7 + i); };
+    auto xr_free = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 9 + i); };
+    auto pr_full = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 11 + i); };
+    auto pr_free = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 13 + i); };
+    const uint32_t done_bar = bar0 + 8u * (2 * kAttnSlots + 15);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     auto slot_addr = [&](int rp) { return sRing + static_cast<uint32_t>(rp % kAttnSlots) * C::SLOT; };
@@ -184,9 +204,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (tid == 0) {
         for (int i = 0; i < kAttnSlots; ++i) { mbar_init(full(i), kAttnProducers); mbar_init(empty(i), 1); }
         mbar_init(q_tm_full, 128);
-        for (int i = 0; i < 2; ++i) { mbar_init(s_full(i), 1); mbar_init(p_full(i), 128); mbar_init(pv_done(i), 1); }
-        mbar_init(x_full, 1);       // the local expect_tx; the peer's bytes complete it
-        mbar_init(x_free, 4);       // one arrive per softmax warp of the peer
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(p_full(i), 128);
+            mbar_init(pv_done(i), 1);
+            mbar_init(xr_full(i), 1);     // a local expect_tx; the peer's bulk copy completes it
+            mbar_init(xr_free(i), 2);     // one arrive per own warp of the peer
+            mbar_init(pr_full(i), 1);
+            mbar_init(pr_free(i), 2);     // one arrive per peer warp of the peer
+        }
         mbar_init(done_bar, 1);
         *s_abort = 0;
         fence_mbar_init();
@@ -284,11 +311,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             auto dK = [&](int rp_) { return sdesc_sw128(slot_addr(rp_), 16, 1024); };
             auto dR = [&](int rp_) { return sdesc_sw64(slot_addr(rp_) + 4 * C::KV_SLOT); };
             auto dV = [&](int rp_) { return sdesc_sw128(slot_addr(rp_), C::KV_SLOT, 1024); };
-            auto issue_qk = [&](int g, int rp_) -> bool {
+            auto issue_qk = [&](int rp_) -> bool {
                 if (!wait_bar(full(rp_ % kAttnSlots), (rp_ / kAttnSlots) & 1, timeout_ns, s_abort)) return false;
                 fence_proxy_async_smem();   // rows written by cp.async, read by the tensor cores
                 tc_fence_after();
-                const uint32_t d = tmem_base + C::TM_SP + (g & 1) * kAttnBK;
+                const uint32_t d = tmem_base + C::TM_S;
                 const uint64_t bk = dK(rp_), br = dR(rp_);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -302,8 +329,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int kk = 0; kk < 2; ++kk)
                     tc_mma_bf16(d, dQR + static_cast<uint64_t>(kk * 2), br + static_cast<uint64_t>(kk * 2),
                                 C::IDESC_QK, 1u);
-                tc_commit(s_full(g & 1));
+                tc_commit(s_full);
                 return true;
+            };
+            auto issue_pv = [&](int g, int rp_, bool first) {
+                const uint64_t bv = dV(rp_);
+#pragma unroll
+                for (int kk = 0; kk < kAttnBK / 16; ++kk)
+                    // V (MN-major): the 4 latent slots are the 64-column chunks (LBO), 8-key groups 1 KB apart
+                    tc_mma_bf16_ts(tmem_base + C::TM_O, tmem_base + C::TM_P + (g & 1) * 32 + kk * 8,
+                                   bv + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::IDESC_PV,
+                                   (!first || kk) ? 1u : 0u);
+                tc_commit(pv_done(g & 1));
+                tc_commit(empty(rp_ % kAttnSlots));
             };
             for (int r = cl; r < rows && ok; r += ncl) {
                 const AttnRow A = attn_row(rs, r, k);
@@ -312,26 +350,42 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ok = wait_bar(q_tm_full, qi & 1, timeout_ns, s_abort);
                 if (!ok) break;
                 tc_fence_after();
-                const int g0 = gi, rp0 = rp;
-                ok = issue_qk(g0, rp0);
-                if (ok && A.nb > 1) ok = issue_qk(g0 + 1, rp0 + 1);
-                for (int i = 0; i < A.nb && ok; ++i) {
-                    const int g = g0 + i;
-                    ok = wait_bar(p_full(g & 1), (g >> 1) & 1, timeout_ns, s_abort);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t bv = dV(rp0 + i);
-#pragma unroll
-                    for (int kk = 0; kk < kAttnBK / 16; ++kk)
-                        // V (MN-major): the 4 latent slots are the 64-column chunks (LBO), 8-key groups 1 KB apart
-                        tc_mma_bf16_ts(tmem_base + C::TM_O, tmem_base + C::TM_SP + (g & 1) * kAttnBK + kk * 8,
-                                       bv + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::IDESC_PV,
-                                       (i | kk) ? 1u : 0u);
-                    tc_commit(pv_done(g & 1));
-                    tc_commit(empty((rp0 + i) % kAttnSlots));
-                    if (i + 2 < A.nb) ok = issue_qk(g + 2, rp0 + i + 2);
+                const int g0 = gi, rp0 = rp, gend = gi + A.nb;
+                ok = issue_qk(rp0);
+                // Q.K^T of block j needs S free (block j-1 read by every lane); P.V of block j
+                // needs its P.  Issue whichever is ready, in block order within each kind.
+                int qk_next = g0 + 1, pv_next = g0;
+                uint64_t t_idle = 0;
+                while (ok && pv_next < gend) {
+                    bool progressed = false;
+                    if (qk_next < gend && mbar_try(s_free, (qk_next - 1) & 1)) {
+                        tc_fence_after();
+                        ok = issue_qk(rp0 + (qk_next - g0));
+                        ++qk_next;
+                        progressed = true;
+                    }
+                    if (ok && pv_next < qk_next && mbar_try(p_full(pv_next & 1), (pv_next >> 1) & 1)) {
+                        tc_fence_after();
+                        issue_pv(pv_next, rp0 + (pv_next - g0), pv_next == g0);
+                        ++pv_next;
+                        progressed = true;
+                    }
+                    if (progressed) {
+                        t_idle = 0;
+                    } else {
+                        const uint64_t now = global_ns();
+                        if (t_idle == 0) {
+                            t_idle = now;
+                        } else if (now - t_idle > timeout_ns) {
+                            *s_abort = 1;
+                            raise_error(DSA_ERR_TIMEOUT);
+                            ok = false;
+                        } else if (*s_abort) {
+                            ok = false;
+                        }
+                    }
                 }
-                gi = g0 + A.nb;
+                gi = gend;
                 rp = rp0 + A.nb;
                 ++qi;
             }
@@ -339,15 +393,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             wait_bar(done_bar, 0, timeout_ns, nullptr);   // before TMEM is released
         }
     } else {
-        // ---------------- softmax / Q items / epilogue (warps 0..3) ----------------
+        // ---------------- softmax group / Q items / epilogue (warps 0..3) ----------------
         const int h = warp * 32 + lane;              // head = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t x_full_peer = mapa(x_full, peer), x_free_peer = mapa(x_free, peer);
-        const uint32_t sX_peer = mapa(sX, peer);
-        const uint8_t* xrow = smem + C::OFF_X + h * 256;
-        uint8_t* xsrow = smem + C::OFF_XS + h * 256;
+        const bool own = (warp >> 1) == rank;         // this lane's head has its softmax here
+        const int hl = h & 63;                        // row of the head in the 64-head exchange tiles
         int qi = 0, gi = 0, rp = 0;
         bool ok = true;
+        uint32_t bulk_pending = 0;                    // this thread has issued bulk copies
 
         // Moves the Q item at ring position rp_ into tensor memory (latent) and the rope buffer.
         auto take_q = [&](int rp_) -> bool {
@@ -388,7 +441,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         auto zero_row = [&](int rr) {   // no valid selection (invalid row): zeros, lse = -inf
             uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<long long>(rr) * kAttnHeads + h) * kAttnDv + rank * 256);
             for (int q = 0; q < 32; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
-            if (lse != nullptr && rank == 0) lse[static_cast<long long>(rr) * kAttnHeads + h] = -INFINITY;
+            if (lse != nullptr && own) lse[static_cast<long long>(rr) * kAttnHeads + h] = -INFINITY;
+        };
+        // Rescales this lane's O row by f (warp-uniform call; f = 1 leaves it unchanged).
+        auto rescale_o = [&](float f) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < 256; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(tmem_base + lane_off + C::TM_O + c0, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+                tmem_st32(tmem_base + lane_off + C::TM_O + c0, o);
+            }
+        };
+        // this warp's P.V of block g-2 has finished reading P buffer g & 1
+        auto wait_p_buffer = [&](int g) -> bool {
+            if (g < 2) return true;
+            return __all_sync(0xffffffffu, wait_bar(pv_done(g & 1), (((g - 2) >> 1) & 1), timeout_ns, s_abort));
         };
 
         // the first query with work
@@ -404,97 +474,159 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ok = take_q(rp);
             rp += 2;
         }
+        const uint32_t rX = mapa(sbase + C::OFF_XR, peer), rP = mapa(sbase + C::OFF_PR, peer);
+        float l_peer = 1.f;                           // peer lanes: the denominator received last
+        // Peer lanes: takes the P of block g (the i-th of the query) that the peer computed for
+        // these heads, rescales these O rows if told to, and hands P to the tensor cores.
+        auto take_p = [&](int g, int i) -> bool {
+            const int b = g & 1;
+            if (hl == 0) mbar_expect_tx(pr_full(b), C::PB);
+            if (!__all_sync(0xffffffffu, wait_bar<true>(pr_full(b), (g >> 1) & 1, timeout_ns, s_abort))) return false;
+            const uint8_t* pm = smem + C::OFF_PR + b * C::PB;
+            const float f = reinterpret_cast<const float*>(pm + C::PB_P)[hl];
+            l_peer = reinterpret_cast<const float*>(pm + C::PB_P + 256)[hl];
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 u = *reinterpret_cast<const uint4*>(pm + hl * 128 + (((c ^ hl) & 7) << 4));
+                pk[4 * c + 0] = u.x; pk[4 * c + 1] = u.y; pk[4 * c + 2] = u.z; pk[4 * c + 3] = u.w;
+            }
+            if (i > 0 && __any_sync(0xffffffffu, f != 1.f)) {
+                // O must hold every earlier P.V before it is rescaled
+                if (!__all_sync(0xffffffffu, wait_bar(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, timeout_ns, s_abort)))
+                    return false;
+                tc_fence_after();
+                rescale_o(f);
+            }
+            if (!wait_p_buffer(g)) return false;
+            tc_fence_after();
+            tmem_st32(tmem_base + lane_off + C::TM_P + b * 32, pk);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(p_full(b));
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa(pr_free(b), peer));   // this warp's rows are read
+            return true;
+        };
         while (r < rows && ok) {
-            float m = -INFINITY, l = 0.f;
+            float m = -INFINITY, l = 0.f;             // own lanes: running max and denominator
             const int g0 = gi;
             for (int i = 0; i < A.nb && ok; ++i) {
                 const int g = g0 + i, b = g & 1;
-                ok = __all_sync(0xffffffffu, wait_bar(s_full(b), (g >> 1) & 1, timeout_ns, s_abort));
+                ok = __all_sync(0xffffffffu, wait_bar(s_full, g & 1, timeout_ns, s_abort));
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t sraw[64];
-                tmem_ld32(tmem_base + lane_off + C::TM_SP + b * kAttnBK, *reinterpret_cast<uint32_t(*)[32]>(sraw));
-                tmem_ld32(tmem_base + lane_off + C::TM_SP + b * kAttnBK + 32,
-                          *reinterpret_cast<uint32_t(*)[32]>(sraw + 32));
+                tmem_ld32(tmem_base + lane_off + C::TM_S, *reinterpret_cast<uint32_t(*)[32]>(sraw));
+                tmem_ld32(tmem_base + lane_off + C::TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(sraw + 32));
                 tmem_ld_wait();
-                // exchange the partial scores with the peer CTA.  x_free: the peer has read
-                // the previous tile, so the previous bulk copy out of XS has completed too.
-                ok = __all_sync(0xffffffffu, wait_bar<true>(x_free, (g & 1) ^ 1, timeout_ns, s_abort));
-                if (!ok) break;
+                tc_fence_before();
+                mbar_arrive(s_free);                   // the next Q.K^T may overwrite S
+                if (!own) {
+                    // ---- peer lanes: send this rank's partial scores of the peer's heads ----
+                    ok = __all_sync(0xffffffffu, wait_bar<true>(xr_free(b), ((g >> 1) & 1) ^ 1, timeout_ns, s_abort));
+                    if (!ok) break;
+                    if (bulk_pending) bulk_wait_read();  // the previous tile has left XS
+                    named_sync(2, 64);
+                    uint8_t* xs = smem + C::OFF_XS + hl * 256;
 #pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    *reinterpret_cast<uint4*>(xsrow + (((c ^ h) & 15) << 4)) =
-                        make_uint4(sraw[4 * c], sraw[4 * c + 1], sraw[4 * c + 2], sraw[4 * c + 3]);
-                fence_proxy_async_smem();
-                named_sync(1, 128);
-                if (h == 0) {
-                    mbar_expect_tx(x_full, C::X_BYTES);
-                    bulk_copy_to_peer(sX_peer, sbase + C::OFF_XS, C::X_BYTES, x_full_peer);
-                }
-                ok = __all_sync(0xffffffffu, wait_bar<true>(x_full, g & 1, timeout_ns, s_abort));
-                if (!ok) break;
-                float sv[64];
+                    for (int c = 0; c < 16; ++c)
+                        *reinterpret_cast<uint4*>(xs + (((c ^ hl) & 15) << 4)) =
+                            make_uint4(sraw[4 * c], sraw[4 * c + 1], sraw[4 * c + 2], sraw[4 * c + 3]);
+                    fence_proxy_async_smem();
+                    named_sync(2, 64);
+                    if (hl == 0) {
+                        bulk_copy_to_peer(rX + b * C::XB, sbase + C::OFF_XS, C::XB, mapa(xr_full(b), peer));
+                        bulk_pending = 1;
+                    }
+                    // ---- then take the P of the PREVIOUS block from the peer, so that sending
+                    // never waits for receiving ----
+                    if (i > 0) ok = take_p(g - 1, i - 1);
+                } else {
+                    // ---- own lanes: complete the scores, softmax, send P ----
+                    if (hl == 0) mbar_expect_tx(xr_full(b), C::XB);
+                    ok = __all_sync(0xffffffffu, wait_bar<true>(xr_full(b), (g >> 1) & 1, timeout_ns, s_abort));
+                    if (!ok) break;
+                    float sv[64];
+                    const uint8_t* xr = smem + C::OFF_XR + b * C::XB + hl * 256;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float4 v = *reinterpret_cast<const float4*>(xrow + (((c ^ h) & 15) << 4));
-                    sv[4 * c + 0] = __uint_as_float(sraw[4 * c + 0]) + v.x;
-                    sv[4 * c + 1] = __uint_as_float(sraw[4 * c + 1]) + v.y;
-                    sv[4 * c + 2] = __uint_as_float(sraw[4 * c + 2]) + v.z;
-                    sv[4 * c + 3] = __uint_as_float(sraw[4 * c + 3]) + v.w;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(x_free_peer);   // this warp's rows of X may be overwritten
-                // columns past the last valid entry are masked (identical for every head)
-                const int nvalid = A.nsel - i * kAttnBK;
-                float mx = -INFINITY;
+                    for (int c = 0; c < 16; ++c) {
+                        const float4 v = *reinterpret_cast<const float4*>(xr + (((c ^ hl) & 15) << 4));
+                        sv[4 * c + 0] = __uint_as_float(sraw[4 * c + 0]) + v.x;
+                        sv[4 * c + 1] = __uint_as_float(sraw[4 * c + 1]) + v.y;
+                        sv[4 * c + 2] = __uint_as_float(sraw[4 * c + 2]) + v.z;
+                        sv[4 * c + 3] = __uint_as_float(sraw[4 * c + 3]) + v.w;
+                    }
+                    // columns past the last valid entry are masked (identical for every head)
+                    const int nvalid = A.nsel - i * kAttnBK;
+                    float mx = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    sv[j] = (j < nvalid) ? sv[j] * scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, sv[j]);
-                }
-                const float m_new = fmaxf(m, mx);
-                const bool resc = m_new > m + 8.f;           // lazy rescale (always true on the first block)
-                const float factor = resc ? fast_exp2(m - m_new) : 1.f;
-                if (i > 0 && __any_sync(0xffffffffu, resc)) {
-                    // O must hold every earlier P.V before it is rescaled
-                    ok = __all_sync(0xffffffffu,
-                                    wait_bar(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, timeout_ns, s_abort));
+                    for (int j = 0; j < 64; ++j) {
+                        sv[j] = (j < nvalid) ? sv[j] * scale_log2 : -INFINITY;
+                        mx = fmaxf(mx, sv[j]);
+                    }
+                    const float m_new = fmaxf(m, mx);
+                    const bool resc = m_new > m + 8.f;       // lazy rescale (always true on the first block)
+                    float factor = resc ? fast_exp2(m - m_new) : 1.f;
+                    if (i == 0) factor = 1.f;                // the first P.V overwrites O
+                    if (resc) {
+                        l *= factor;
+                        m = m_new;
+                    }
+                    // P = 2^(z - m) in bf16 (pairs of keys per 32-bit column); l sums the rounded values
+                    uint32_t pk[32];
+                    float lsum = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const __nv_bfloat162 pr = __floats2bfloat162_rn(fast_exp2(sv[2 * j] - m), fast_exp2(sv[2 * j + 1] - m));
+                        const float2 back = __bfloat1622float2(pr);
+                        lsum += back.x + back.y;
+                        pk[j] = *reinterpret_cast<const uint32_t*>(&pr);
+                    }
+                    l += lsum;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(mapa(xr_free(b), peer));   // this warp's rows are read
+                    // send P, the rescale factor and the denominator to the peer
+                    ok = __all_sync(0xffffffffu, wait_bar<true>(pr_free(b), ((g >> 1) & 1) ^ 1, timeout_ns, s_abort));
+                    if (!ok) break;
+                    if (bulk_pending) bulk_wait_read();  // the previous message has left PS
+                    named_sync(3, 64);
+                    uint8_t* ps = smem + C::OFF_PS;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(ps + hl * 128 + (((c ^ hl) & 7) << 4)) =
+                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    reinterpret_cast<float*>(ps + C::PB_P)[hl] = factor;
+                    reinterpret_cast<float*>(ps + C::PB_P + 256)[hl] = l;
+                    fence_proxy_async_smem();
+                    named_sync(3, 64);
+                    if (hl == 0) {
+                        bulk_copy_to_peer(rP + b * C::PB, sbase + C::OFF_PS, C::PB, mapa(pr_full(b), peer));
+                        bulk_pending = 1;
+                    }
+                    if (i > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+                        ok = __all_sync(0xffffffffu,
+                                        wait_bar(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, timeout_ns, s_abort));
+                        if (!ok) break;
+                        tc_fence_after();
+                        rescale_o(factor);
+                    }
+                    ok = wait_p_buffer(g);
                     if (!ok) break;
                     tc_fence_after();
-#pragma unroll 1
-                    for (int c0 = 0; c0 < 256; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(tmem_base + lane_off + C::TM_O + c0, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * factor);
-                        tmem_st32(tmem_base + lane_off + C::TM_O + c0, o);
-                    }
+                    tmem_st32(tmem_base + lane_off + C::TM_P + b * 32, pk);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(p_full(b));
                 }
-                if (resc) {
-                    l *= factor;
-                    m = m_new;
-                }
-                // P = 2^(z - m) in bf16 (pairs of keys per 32-bit column); l sums the rounded values
-                uint32_t pk[32];
-                float lsum = 0.f;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(fast_exp2(sv[2 * j] - m), fast_exp2(sv[2 * j + 1] - m));
-                    const float2 back = __bfloat1622float2(pr);
-                    lsum += back.x + back.y;
-                    pk[j] = *reinterpret_cast<const uint32_t*>(&pr);
-                }
-                l += lsum;
-                tmem_st32(tmem_base + lane_off + C::TM_SP + b * kAttnBK, pk);
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(p_full(b));
             }
+            if (ok && !own) ok = take_p(g0 + A.nb - 1, A.nb - 1);
             if (!ok) break;
             gi = g0 + A.nb;
             rp += A.nb;
             const int r_cur = r;
+            const float l_fin = own ? l : l_peer;
+            const float m_fin = m;
             // next query with work; its Q goes into tensor memory now (every Q.K^T of this
             // query has completed: the last s_full was observed above)
             r += ncl;
@@ -514,7 +646,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ok = ok && __all_sync(0xffffffffu, wait_bar(pv_done(gl & 1), (gl >> 1) & 1, timeout_ns, s_abort));
             if (!ok) break;
             tc_fence_after();
-            const float inv = 1.f / l;
+            const float inv = 1.f / l_fin;
             const long long orow = (static_cast<long long>(r_cur) * kAttnHeads + h) * kAttnDv + rank * 256;
 #pragma unroll 1
             for (int c0 = 0; c0 < 256; c0 += 32) {
@@ -534,10 +666,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
-            if (lse != nullptr && rank == 0)
-                lse[static_cast<long long>(r_cur) * kAttnHeads + h] = (m + log2f(l)) * 0.69314718055994530942f;
+            if (lse != nullptr && own)
+                lse[static_cast<long long>(r_cur) * kAttnHeads + h] = (m_fin + log2f(l_fin)) * 0.69314718055994530942f;
             tc_fence_before();   // O has been read before the next query's first P.V overwrites it
         }
+        if (bulk_pending) bulk_wait_read();
         (void)qi;
     }
 
