@@ -109,6 +109,23 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _attn_traffic(cfg):
+    """DRAM bytes per attention launch from the committed ncu summary, or None when the
+    kernel source has changed since the counters were taken (or for other workloads)."""
+    import hashlib
+
+    if cfg.name != "long":
+        return None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)["attn_tc_kernel_long"]
+        with open(os.path.join(ROOT, "sparse_attention_long_gemm_b300", "csrc", "attn_tc.cuh"), "rb") as f:
+            sha = hashlib.sha1(f.read()).hexdigest()
+    except (OSError, ValueError, KeyError):
+        return None
+    return rec["bytes_per_launch"] if rec.get("source_sha1") == sha else None
+
+
 def _cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -325,12 +342,7 @@ def run_ours(args, cfg):
     topk_gbs = topk_bytes / (stage_ms[1] * 1e-3) / 1e9
     attn_tf = selected * FLOP_PER_PAIR_ATTN / (stage_ms[2] * 1e-3) / 1e12
     peak_t = peaks["bf16_tflops_sustained"]
-    traffic = None
-    try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            traffic = json.load(f).get("attn_tc_kernel_long")
-    except (OSError, ValueError):
-        traffic = None
+    traffic = _attn_traffic(cfg)
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, args)
