@@ -82,6 +82,7 @@ int device_info(DevInfo** out) {
         set(reinterpret_cast<const void*>(&indexer_tc_kernel<kPreNQ, kPreKS, kPreQB>), IdxTc<kPreNQ, kPreKS, kPreQB>::SMEM);
         set(reinterpret_cast<const void*>(&indexer_tc_kernel<kDecNQ, kDecKS, kDecQB>), IdxTc<kDecNQ, kDecKS, kDecQB>::SMEM);
         set(reinterpret_cast<const void*>(&attn_tc_kernel), AttnTc::SMEM);
+        set(reinterpret_cast<const void*>(&topk_smem_kernel), topk_smem_bytes(kTopkSmemKeys));
         set(reinterpret_cast<const void*>(&indexer_simt_kernel<float>), indexer_simt_smem(128, 128));
         set(reinterpret_cast<const void*>(&indexer_simt_kernel<__nv_bfloat16>), indexer_simt_smem(128, 128));
         set(reinterpret_cast<const void*>(&attn_simt_kernel<float>), attn_simt_smem(1024, 16384));
@@ -166,7 +167,11 @@ int run_index_scores(const dsa_params* p, const void* q_idx, const float* w, con
 
 int run_topk(const dsa_params* p, const float* scores, long long ld, const RowSpec& rs, int rows, int* idx,
              cudaStream_t st) {
-    topk_kernel<<<rows, kTopkThreads, 0, st>>>(rs, scores, ld, p->topk, idx);
+    if (rs.max_len <= kTopkSmemKeys) {
+        topk_smem_kernel<<<rows, kTopkThreads, topk_smem_bytes(rs.max_len), st>>>(rs, scores, ld, p->topk, idx);
+    } else {
+        topk_kernel<<<rows, kTopkThreads, 0, st>>>(rs, scores, ld, p->topk, idx);
+    }
     return launch_status();
 }
 

@@ -11,12 +11,15 @@
 // the per-head scores never leave TMEM and no cross-lane reduction is
 // needed.  Only the causal part (s <= t) is computed and written.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over work units):
+// Warp roles (320 threads, one CTA per SM, persistent over work units):
 //   warp 0      TMA producer: query block (NQ*64 rows x 128, once per unit)
 //               and key tiles (128 x 128) into 128B-swizzled shared memory;
 //   warp 1      allocates TMEM and issues tcgen05.mma (one thread);
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, ReLU, w-sum,
-//               coalesced fp32 stores of the score rows.
+//   warps 2..9  epilogue: two warps per TMEM lane quadrant, each taking half
+//               of the block's queries; both queries' accumulator columns are
+//               loaded before one wait, and each 64-head sum runs as four
+//               independent partial sums, so the epilogue keeps up with the
+//               MMAs instead of serialising load latency and FMA chains.
 // Two TMEM accumulators alternate so the epilogue of one key tile overlaps
 // the MMAs of the next.
 //
@@ -35,7 +38,8 @@ namespace dsa {
 constexpr int kIdxHeads = 64;
 constexpr int kIdxDim = 128;
 constexpr int kIdxTileKeys = 128;
-constexpr int kIdxTcThreads = 192;
+constexpr int kIdxTcThreads = 320;
+constexpr int kIdxEpiThreads = 256;      // warps 2..9
 constexpr int kIdxTcMaxBatch = 256;
 
 template <int NQ, int KSTAGES, int QBUF>
@@ -155,7 +159,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid == 0) {
         for (int i = 0; i < QBUF; ++i) { mbar_init(q_full(i), 1); mbar_init(q_empty(i), 1); }
         for (int i = 0; i < KSTAGES; ++i) { mbar_init(k_full(i), 1); mbar_init(k_empty(i), 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(acc_full(i), 1); mbar_init(acc_empty(i), 128); }
+        for (int i = 0; i < 2; ++i) { mbar_init(acc_full(i), 1); mbar_init(acc_empty(i), kIdxEpiThreads); }
         mbar_init(done_bar, 1);
         *s_abort = 0;
         fence_mbar_init();
@@ -256,6 +260,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     } else if (warp >= 2) {
         // ---------------- epilogue ----------------
         const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;          // which half of the block's queries
+        constexpr int QPH = (NQ + 1) / 2;          // queries per half
         const int row = quad * 32 + lane;          // key within the tile = TMEM lane
         int it_acc = 0;
         bool ok = true;
@@ -267,34 +273,34 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (!ok) break;
                 tc_fence_after();
                 const int s = kt * kIdxTileKeys + row;
-#pragma unroll 1
-                for (int qi = 0; qi < NQ; ++qi) {
-                    if (qi >= U.nq) break;     // warp-uniform
-                    uint32_t v0[32], v1[32];
-                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                           static_cast<uint32_t>(ab * C::BN + qi * kIdxHeads);
-                    tmem_ld32(taddr, v0);
-                    tmem_ld32(taddr + 32, v1);
+                const int q0 = half * QPH;
+                if (q0 < U.nq) {   // warp-uniform
+                    uint32_t v[QPH][64];
+#pragma unroll
+                    for (int qq = 0; qq < QPH; ++qq) {
+                        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                               static_cast<uint32_t>(ab * C::BN + (q0 + qq) * kIdxHeads);
+                        tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(v[qq]));
+                        tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(v[qq] + 32));
+                    }
                     tmem_ld_wait();
-                    const float4* w4 = reinterpret_cast<const float4*>(w + static_cast<long long>(U.q_row0 + qi) * kIdxHeads);
-                    float acc = 0.f;
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 ww = __ldg(w4 + j4);
-                        acc = fmaf(ww.x, fmaxf(__uint_as_float(v0[4 * j4 + 0]), 0.f), acc);
-                        acc = fmaf(ww.y, fmaxf(__uint_as_float(v0[4 * j4 + 1]), 0.f), acc);
-                        acc = fmaf(ww.z, fmaxf(__uint_as_float(v0[4 * j4 + 2]), 0.f), acc);
-                        acc = fmaf(ww.w, fmaxf(__uint_as_float(v0[4 * j4 + 3]), 0.f), acc);
-                    }
+                    for (int qq = 0; qq < QPH; ++qq) {
+                        const int qi = q0 + qq;
+                        if (qi >= U.nq) break;     // warp-uniform
+                        const float4* w4 = reinterpret_cast<const float4*>(w + static_cast<long long>(U.q_row0 + qi) * kIdxHeads);
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 ww = __ldg(w4 + 8 + j4);
-                        acc = fmaf(ww.x, fmaxf(__uint_as_float(v1[4 * j4 + 0]), 0.f), acc);
-                        acc = fmaf(ww.y, fmaxf(__uint_as_float(v1[4 * j4 + 1]), 0.f), acc);
-                        acc = fmaf(ww.z, fmaxf(__uint_as_float(v1[4 * j4 + 2]), 0.f), acc);
-                        acc = fmaf(ww.w, fmaxf(__uint_as_float(v1[4 * j4 + 3]), 0.f), acc);
+                        for (int j4 = 0; j4 < 16; ++j4) {
+                            const float4 ww = __ldg(w4 + j4);
+                            acc[0] = fmaf(ww.x, fmaxf(__uint_as_float(v[qq][4 * j4 + 0]), 0.f), acc[0]);
+                            acc[1] = fmaf(ww.y, fmaxf(__uint_as_float(v[qq][4 * j4 + 1]), 0.f), acc[1]);
+                            acc[2] = fmaf(ww.z, fmaxf(__uint_as_float(v[qq][4 * j4 + 2]), 0.f), acc[2]);
+                            acc[3] = fmaf(ww.w, fmaxf(__uint_as_float(v[qq][4 * j4 + 3]), 0.f), acc[3]);
+                        }
+                        if (s <= U.t0 + qi)
+                            scores[static_cast<long long>(U.q_row0 + qi) * ld + s] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
                     }
-                    if (s <= U.t0 + qi) scores[static_cast<long long>(U.q_row0 + qi) * ld + s] = acc;
                 }
                 tc_fence_before();
                 mbar_arrive(acc_empty(ab));

@@ -5,8 +5,17 @@
 // (all of them when there are at most index_topk).  Equal scores go to the
 // lower position.  Output: ascending positions, -1 padded.
 //
-// One CTA (1024 threads) per row.  Scores become order-preserving 32-bit
-// keys (score_key).  Three histogram passes over 11 + 11 + 10 key bits
+// topk_smem_kernel (rows of at most kTopkSmemKeys positions): one CTA of 1024
+// threads per row reads the row from HBM ONCE, keeping its keys in shared
+// memory, so the two refining radix passes and the emit pass cost a few
+// shared-memory instructions per element instead of global re-reads and
+// block-wide scans per 4096 elements: the emit pass gives each warp a
+// contiguous segment of positions, counts per warp, scans the 32 warp counts
+// once, and writes each warp's selections in order with ballots.
+//
+// topk_kernel (any row length; used for rows longer than the shared-memory
+// capacity, e.g. long decode caches): one CTA (1024 threads) per row.  Scores
+// become order-preserving 32-bit keys (score_key).  Three histogram passes over 11 + 11 + 10 key bits
 // find the exact key T of the k-th largest score and how many of the
 // scores equal to T must be kept ("need"); a final pass in position order
 // keeps every key > T and the first `need` keys == T, computing output
@@ -153,6 +162,133 @@ topk_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int k, i
         }
         sel_seen += gt_tot + min(eq_tot, rem);
         eq_seen += eq_tot;
+    }
+}
+
+constexpr int kTopkSmemKeys = 50 * 1024;   // keys held in shared memory (200 KB)
+constexpr int kTopkBins = 2048;
+
+__host__ __device__ constexpr size_t topk_smem_bytes(int max_len) {
+    return static_cast<size_t>((max_len + 3) / 4 * 4) * 4 + kTopkBins * 4 + 64 * 4 + 64;
+}
+
+__global__ void __launch_bounds__(kTopkThreads)
+topk_smem_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int k, int* __restrict__ idx_out) {
+    extern __shared__ __align__(16) uint8_t tk_smem[];
+    const int n_cap = (rs.max_len + 3) / 4 * 4;
+    uint32_t* keys = reinterpret_cast<uint32_t*>(tk_smem);
+    uint32_t* hist = keys + n_cap;
+    uint32_t* s_cnt = hist + kTopkBins;            // [32] gt counts, [32] eq counts per warp
+    uint32_t* s_misc = s_cnt + 64;                 // digit, above
+
+    const int r = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    int* out = idx_out + static_cast<long long>(r) * k;
+    const RowInfo ri = row_info(rs, r);
+    const int n = ri.ok ? ri.n : 0;
+    if (n <= k) {  // every candidate is kept (or the row is invalid: all -1)
+        for (int i = tid; i < k; i += kTopkThreads) out[i] = (i < n) ? i : -1;
+        return;
+    }
+    const float4* row4 = reinterpret_cast<const float4*>(scores + static_cast<long long>(r) * ld);
+    const int n4 = (n + 3) >> 2;
+    uint4* keys4 = reinterpret_cast<uint4*>(keys);
+
+    // pass 1: the only read of the row (HBM): keys to shared memory, histogram of the top 11 bits
+    for (int i = tid; i < kTopkBins; i += kTopkThreads) hist[i] = 0u;
+    __syncthreads();
+    for (int i4 = tid; i4 < n4; i4 += kTopkThreads) {
+        const float4 v = __ldcs(row4 + i4);        // streamed: every score is read once
+        uint4 kk = make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+        const int base = i4 * 4;
+        if (base + 3 >= n) {   // the row's ragged tail: positions past n rank below everything
+            if (base + 1 >= n) kk.y = 0u;
+            if (base + 2 >= n) kk.z = 0u;
+            if (base + 3 >= n) kk.w = 0u;
+        }
+        keys4[i4] = kk;
+        atomicAdd(&hist[kk.x >> 21], 1u);
+        if (base + 1 < n) atomicAdd(&hist[kk.y >> 21], 1u);
+        if (base + 2 < n) atomicAdd(&hist[kk.z >> 21], 1u);
+        if (base + 3 < n) atomicAdd(&hist[kk.w >> 21], 1u);
+    }
+    __syncthreads();
+
+    uint32_t prefix = 0, need = static_cast<uint32_t>(k);
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = (pass == 0) ? 21 : (pass == 1 ? 10 : 0);
+        const int bits = (pass == 2) ? 10 : 11;
+        const int nb = 1 << bits;
+        if (pass > 0) {
+            // histogram of the next digit over the keys that match the prefix found so far
+            const int hi_shift = shift + bits;
+            for (int i = tid; i < nb; i += kTopkThreads) hist[i] = 0u;
+            __syncthreads();
+            const uint32_t mask = static_cast<uint32_t>(nb - 1);
+            for (int i4 = tid; i4 < n4; i4 += kTopkThreads) {
+                const uint4 kk = keys4[i4];
+                const int base = i4 * 4;
+                if ((kk.x >> hi_shift) == prefix) atomicAdd(&hist[(kk.x >> shift) & mask], 1u);
+                if ((kk.y >> hi_shift) == prefix && base + 1 < n) atomicAdd(&hist[(kk.y >> shift) & mask], 1u);
+                if ((kk.z >> hi_shift) == prefix && base + 2 < n) atomicAdd(&hist[(kk.z >> shift) & mask], 1u);
+                if ((kk.w >> hi_shift) == prefix && base + 3 < n) atomicAdd(&hist[(kk.w >> shift) & mask], 1u);
+            }
+            __syncthreads();
+        }
+        // the bin that holds the need-th largest key (thread t owns bins from the top)
+        const int per = nb / kTopkThreads;   // 2 or 1
+        uint32_t cnt[2] = {0u, 0u};
+        for (int e = 0; e < per; ++e) cnt[e] = hist[nb - 1 - tid * per - e];
+        uint32_t tot;
+        uint32_t above = block_excl_scan(cnt[0] + cnt[1], s_cnt, &tot);
+        for (int e = 0; e < per; ++e) {
+            if (above < need && need <= above + cnt[e]) {
+                s_misc[0] = static_cast<uint32_t>(nb - 1 - tid * per - e);
+                s_misc[1] = above;
+            }
+            above += cnt[e];
+        }
+        __syncthreads();
+        prefix = (prefix << bits) | s_misc[0];
+        need -= s_misc[1];
+        __syncthreads();
+    }
+    const uint32_t T = prefix;   // key of the k-th largest score; `need` keys equal to T are kept
+
+    // emit: warp w owns positions [w*seg, (w+1)*seg); count, scan the warp counts, write in order
+    const int seg = ((n4 + 31) / 32) * 4;
+    const int p0 = wid * seg, p1 = min(n, p0 + seg);
+    uint32_t c_gt = 0, c_eq = 0;
+    for (int p = p0 + lane; p < p1; p += 32) {
+        const uint32_t kk = keys[p];
+        c_gt += (kk > T) ? 1u : 0u;
+        c_eq += (kk == T) ? 1u : 0u;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        c_gt += __shfl_xor_sync(0xffffffffu, c_gt, o);
+        c_eq += __shfl_xor_sync(0xffffffffu, c_eq, o);
+    }
+    if (lane == 0) { s_cnt[wid] = c_gt; s_cnt[32 + wid] = c_eq; }
+    __syncthreads();
+    uint32_t gt_before = 0, eq_before = 0;
+    for (int w = 0; w < wid; ++w) { gt_before += s_cnt[w]; eq_before += s_cnt[32 + w]; }
+    for (int base = p0; base < p1; base += 32) {
+        const int p = base + lane;
+        const uint32_t kk = (p < p1) ? keys[p] : 0u;
+        const bool gt = (p < p1) && kk > T;
+        const bool eq = (p < p1) && kk == T;
+        const uint32_t mgt = __ballot_sync(0xffffffffu, gt), meq = __ballot_sync(0xffffffffu, eq);
+        const uint32_t lt_mask = (1u << lane) - 1u;
+        const uint32_t my_eq = eq_before + __popc(meq & lt_mask);       // equal keys before p
+        const bool take = gt || (eq && my_eq < need);
+        if (take) {
+            const uint32_t slot = gt_before + __popc(mgt & lt_mask) + min(my_eq, need);
+            out[slot] = p;
+        }
+        gt_before += __popc(mgt);
+        eq_before += __popc(meq);
     }
 }
 
