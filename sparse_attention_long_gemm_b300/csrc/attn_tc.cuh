@@ -45,7 +45,8 @@
 // rest holds the exchange buffers (received tiles double-buffered, outgoing
 // tiles staged once and sent by one bulk copy each).
 //
-// Per CTA (224 threads):
+// Per CTA (256 threads; the warp of a role depends on the rank so that the two
+// warps running the softmax have their SM sub-partitions to themselves):
 //   warps 0..3  softmax group, one head (TMEM lane) per thread.  The two
 //               warps whose lanes are this rank's heads ("own" warps)
 //               complete their scores, run the online softmax (running max
@@ -55,10 +56,11 @@
 //               heads into tensor memory, rescaling those O rows first when
 //               told to.  All four move Q items into tensor memory and run
 //               the output epilogue;
-//   warp 4      TMEM allocation and tcgen05.mma issue (one thread, polling
+//   one warp    TMEM allocation and tcgen05.mma issue (one thread, polling
 //               both the next Q.K^T and the next P.V so neither waits on the
-//               other);
-//   warps 5..6  producers: the rows of a KV item by cp.async, each warp
+//               other): warp 6 on rank 0, warp 4 on rank 1;
+//   one warp    producer (warp 7 on rank 0, warp 5 on rank 1; the other two
+//               warps of 4..7 are idle): the rows of a KV item by cp.async, each warp
 //               instruction one key's 512 latent bytes (the rope parts of 8
 //               keys per instruction), completion signalled with
 //               cp.async.mbarrier.arrive.noinc so the producers never wait for
@@ -77,8 +79,8 @@ constexpr int kAttnDqk = 576;
 constexpr int kAttnDv = 512;
 constexpr int kAttnBK = 64;              // selected keys per block
 constexpr int kAttnSlots = 4;            // ring slots
-constexpr int kAttnThreads = 224;
-constexpr int kAttnProducers = 64;       // threads of warps 5..6
+constexpr int kAttnThreads = 256;
+constexpr int kAttnProducers = 32;       // threads of the producer warp
 
 struct AttnTc {
     static constexpr int KV_SLOT = kAttnBK * 128;                   // 64 keys x 64 latent cols = 8 KB
@@ -155,6 +157,14 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// Arrive on an mbarrier of the peer CTA without release semantics.  Used where
+// the only accesses to order are this thread's earlier shared-memory loads of
+// the buffer being released, whose values have already been consumed by
+// instructions before the arrive (so the loads have completed).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
 // Rows of one query: number of valid selected entries and of 64-key blocks.
 struct AttnRow {
     RowInfo ri;
@@ -200,6 +210,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int rank = static_cast<int>(cluster_ctarank());
     const int peer = rank ^ 1;
     const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    // Warps w and w+4 share an SM sub-partition; the softmax ("own") warps are 0,1 on rank 0
+    // and 2,3 on rank 1, so the MMA and producer warps go to the other two sub-partitions.
+    const int mma_warp = (rank == 0) ? 6 : 4;
+    const int prod_warp = (rank == 0) ? 7 : 5;
 
     if (tid == 0) {
         for (int i = 0; i < kAttnSlots; ++i) { mbar_init(full(i), kAttnProducers); mbar_init(empty(i), 1); }
@@ -220,7 +234,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_q_rope);
     }
-    if (warp == 4) {
+    if (warp == mma_warp) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -230,10 +244,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp >= 5) {
-        // ---------------- producers: Q items (TMA) and KV items (cp.async) ----------------
-        const int pt = tid - 5 * 32;                 // 0..63
-        const int pw = pt >> 5;                      // which half of the block's keys
+    if (warp == prod_warp) {
+        // ---------------- producer: Q items (TMA) and KV items (cp.async) ----------------
+        const int pt = lane;
         int rp = 0;
         bool ok = true;
         for (int r = cl; r < rows && ok; r += ncl) {
@@ -260,39 +273,50 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // KV items
             const int* irow = idx + static_cast<long long>(r) * k;
             const long long kb = A.ri.key_base;
-            const int kown = pw * 32 + lane;         // key of the block whose index this thread loads
-            int e0, e1, e2, e3;
-            auto ld_ent = [&](int i) {
-                const int ent = i * kAttnBK + kown;
-                return (ent < A.nsel) ? __ldg(irow + ent) : 0;
-            };
-            e0 = ld_ent(0); e1 = ld_ent(1); e2 = ld_ent(2); e3 = ld_ent(3);
-            for (int i = 0; i < A.nb && ok; ++i, ++rp) {
-                int s = e0;
-                if (s < 0 || s >= A.ri.n) {
-                    if (i * kAttnBK + kown < A.nsel) raise_error(DSA_ERR_DEVICE_DATA);
-                    s = 0;   // any in-range row; entries past nsel are masked by the softmax
+            // lane l loads the indices of keys l and l+32 of each block, four blocks ahead
+            int e0[2], e1[2], e2[2], e3[2];
+            auto ld_ent = [&](int i, int (&v)[2]) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int ent = i * kAttnBK + hh * 32 + lane;
+                    v[hh] = (ent < A.nsel) ? __ldg(irow + ent) : 0;
                 }
-                const long long myrow = kb + s;
-                e0 = e1; e1 = e2; e2 = e3; e3 = ld_ent(i + 4);
+            };
+            ld_ent(0, e0); ld_ent(1, e1); ld_ent(2, e2); ld_ent(3, e3);
+            for (int i = 0; i < A.nb && ok; ++i, ++rp) {
+                long long myrow[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    int s = e0[hh];
+                    if (s < 0 || s >= A.ri.n) {
+                        if (i * kAttnBK + hh * 32 + lane < A.nsel) raise_error(DSA_ERR_DEVICE_DATA);
+                        s = 0;   // any in-range row; entries past nsel are masked by the softmax
+                    }
+                    myrow[hh] = kb + s;
+                    e0[hh] = e1[hh]; e1[hh] = e2[hh]; e2[hh] = e3[hh];
+                }
+                ld_ent(i + 4, e3);
                 ok = wait_bar(empty(rp % kAttnSlots), ((rp / kAttnSlots) & 1) ^ 1, timeout_ns, s_abort);
                 if (!ok) break;
                 const uint32_t st = slot_addr(rp);
                 // latent: one key (512 contiguous bytes) per warp instruction
                 const int j = lane >> 3, c = lane & 7;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll 8
-                for (int kk = 0; kk < 32; ++kk) {
-                    const long long row = __shfl_sync(0xffffffffu, myrow, kk);
-                    const int key = pw * 32 + kk;
-                    cp_async_16(st + j * C::KV_SLOT + key * 128 + (((c ^ key) & 7) << 4),
-                                kv + row * kAttnDqk + rank * 256 + lane * 8);
+                    for (int kk = 0; kk < 32; ++kk) {
+                        const long long row = __shfl_sync(0xffffffffu, myrow[hh], kk);
+                        const int key = hh * 32 + kk;
+                        cp_async_16(st + j * C::KV_SLOT + key * 128 + (((c ^ key) & 7) << 4),
+                                    kv + row * kAttnDqk + rank * 256 + lane * 8);
+                    }
                 }
                 // rope: 8 keys (64 bytes each) per warp instruction
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int kl = t * 8 + (lane >> 2), cc = lane & 3;
-                    const long long row = __shfl_sync(0xffffffffu, myrow, kl);
-                    const int key = pw * 32 + kl;
+                for (int t = 0; t < 8; ++t) {
+                    const int kl = (t & 3) * 8 + (lane >> 2), cc = lane & 3;
+                    const long long row = __shfl_sync(0xffffffffu, myrow[t >> 2], kl);
+                    const int key = (t >> 2) * 32 + kl;
                     cp_async_16(st + 4 * C::KV_SLOT + key * 64 + (((cc ^ (key >> 1)) & 3) << 4),
                                 kv + row * kAttnDqk + 512 + rank * 32 + cc * 8);
                 }
@@ -301,7 +325,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         cp_async_wait<0>();
         if (!ok) sleep_ns(2000000ull);  // let copies already issued land before the CTA exits
-    } else if (warp == 4) {
+    } else if (warp == mma_warp) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             int qi = 0, gi = 0, rp = 0;
@@ -392,7 +416,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_commit(done_bar);                          // every MMA issued has completed
             wait_bar(done_bar, 0, timeout_ns, nullptr);   // before TMEM is released
         }
-    } else {
+    } else if (warp < 4) {
         // ---------------- softmax group / Q items / epilogue (warps 0..3) ----------------
         const int h = warp * 32 + lane;              // head = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
@@ -559,11 +583,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                     // columns past the last valid entry are masked (identical for every head)
                     const int nvalid = A.nsel - i * kAttnBK;
-                    float mx = -INFINITY;
+                    if (nvalid < kAttnBK) {
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        sv[j] = (j < nvalid) ? sv[j] * scale_log2 : -INFINITY;
-                        mx = fmaxf(mx, sv[j]);
+                        for (int j = 0; j < 64; ++j)
+                            if (j >= nvalid) sv[j] = -INFINITY;
+                    }
+                    // With a positive scale the row maximum is taken on the raw scores and the
+                    // scale is folded into the exponent's FMA (one instruction per score).
+                    const bool pos_scale = scale_log2 > 0.f;
+                    float mx = -INFINITY;
+                    if (pos_scale) {
+                        float t8[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) t8[q] = sv[q];
+#pragma unroll
+                        for (int j = 8; j < 64; ++j) t8[j & 7] = fmaxf(t8[j & 7], sv[j]);
+                        mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
+                                   fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+                        mx *= scale_log2;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) {
+                            sv[j] = (j < nvalid) ? sv[j] * scale_log2 : -INFINITY;
+                            mx = fmaxf(mx, sv[j]);
+                        }
                     }
                     const float m_new = fmaxf(m, mx);
                     const bool resc = m_new > m + 8.f;       // lazy rescale (always true on the first block)
@@ -574,18 +617,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         m = m_new;
                     }
                     // P = 2^(z - m) in bf16 (pairs of keys per 32-bit column); l sums the rounded values
+                    const float zs = pos_scale ? scale_log2 : 1.f;
                     uint32_t pk[32];
                     float lsum = 0.f;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const __nv_bfloat162 pr = __floats2bfloat162_rn(fast_exp2(sv[2 * j] - m), fast_exp2(sv[2 * j + 1] - m));
+                        const __nv_bfloat162 pr = __floats2bfloat162_rn(fast_exp2(fmaf(sv[2 * j], zs, -m)),
+                                                                        fast_exp2(fmaf(sv[2 * j + 1], zs, -m)));
                         const float2 back = __bfloat1622float2(pr);
                         lsum += back.x + back.y;
                         pk[j] = *reinterpret_cast<const uint32_t*>(&pr);
                     }
                     l += lsum;
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(mapa(xr_free(b), peer));   // this warp's rows are read
+                    if (lane == 0) mbar_arrive_cluster_relaxed(mapa(xr_free(b), peer));   // this warp's rows are read
                     // send P, the rescale factor and the denominator to the peer
                     ok = __all_sync(0xffffffffu, wait_bar<true>(pr_free(b), ((g >> 1) & 1) ^ 1, timeout_ns, s_abort));
                     if (!ok) break;
@@ -677,7 +722,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_before();
     __syncthreads();
     cluster_sync();             // the peer no longer writes into this CTA's shared memory
-    if (warp == 4) {
+    if (warp == mma_warp) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
