@@ -42,6 +42,21 @@ constexpr int kIdxTcThreads = 320;
 constexpr int kIdxEpiThreads = 256;      // warps 2..9
 constexpr int kIdxTcMaxBatch = 256;
 
+// Packed fp32 pairs (sm_100 family): d = a * b + c on both halves at once.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t x, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 template <int NQ, int KSTAGES, int QBUF>
 struct IdxTc {
     static constexpr int BN = NQ * kIdxHeads;                 // MMA N
@@ -289,15 +304,23 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         const int qi = q0 + qq;
                         if (qi >= U.nq) break;     // warp-uniform
                         const float4* w4 = reinterpret_cast<const float4*>(w + static_cast<long long>(U.q_row0 + qi) * kIdxHeads);
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        // ReLU per head, then the w-weighted sum as packed fp32x2 FMAs (two heads per
+                        // instruction), in two independent pairs of partial sums
+                        uint64_t acc2[2] = {0ull, 0ull};
 #pragma unroll
                         for (int j4 = 0; j4 < 16; ++j4) {
                             const float4 ww = __ldg(w4 + j4);
-                            acc[0] = fmaf(ww.x, fmaxf(__uint_as_float(v[qq][4 * j4 + 0]), 0.f), acc[0]);
-                            acc[1] = fmaf(ww.y, fmaxf(__uint_as_float(v[qq][4 * j4 + 1]), 0.f), acc[1]);
-                            acc[2] = fmaf(ww.z, fmaxf(__uint_as_float(v[qq][4 * j4 + 2]), 0.f), acc[2]);
-                            acc[3] = fmaf(ww.w, fmaxf(__uint_as_float(v[qq][4 * j4 + 3]), 0.f), acc[3]);
+                            const uint64_t wa = pack_f32x2(ww.x, ww.y), wb = pack_f32x2(ww.z, ww.w);
+                            const uint64_t va = pack_f32x2(fmaxf(__uint_as_float(v[qq][4 * j4 + 0]), 0.f),
+                                                           fmaxf(__uint_as_float(v[qq][4 * j4 + 1]), 0.f));
+                            const uint64_t vb = pack_f32x2(fmaxf(__uint_as_float(v[qq][4 * j4 + 2]), 0.f),
+                                                           fmaxf(__uint_as_float(v[qq][4 * j4 + 3]), 0.f));
+                            acc2[0] = fma_f32x2(wa, va, acc2[0]);
+                            acc2[1] = fma_f32x2(wb, vb, acc2[1]);
                         }
+                        float acc[4];
+                        unpack_f32x2(acc2[0], acc[0], acc[1]);
+                        unpack_f32x2(acc2[1], acc[2], acc[3]);
                         if (s <= U.t0 + qi)
                             scores[static_cast<long long>(U.q_row0 + qi) * ld + s] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
                     }
