@@ -53,6 +53,22 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(ms, ws, device):
+    """The slowest rank's time (every rank gets it): the job is as fast as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(units_per_rank, ws, ms_max):
+    """Whole-job throughput: every rank processed units_per_rank in at most ms_max."""
+    return units_per_rank * ws / (ms_max / 1e3)
+
+
 def _workload_desc(cfg, lens):
     return (f"{cfg.name} prefill: B={len(lens)}, L={max(lens)} causal, indexer {cfg.n_idx_heads}x{cfg.idx_dim}, "
             f"index_topk={cfg.topk}, MLA {cfg.n_heads} heads {cfg.d_qk}/{cfg.d_v}, {cfg.dtype}")
@@ -286,10 +302,7 @@ def run_ours(args, cfg):
     st = [[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs]
     step_ms = sum(sum(x) for x in st) / args.steps
     stage_ms = [sum(x[i] for x in st) / args.steps for i in range(3)]
-    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    step_ms_max = float(t.item())
+    step_ms_max = max_over_ranks(step_ms, ws, dev)
 
     # ---- end to end: host buffers, H2D + fused dsa_forward + D2H inside the timed region ----
     e2e = None
@@ -322,10 +335,8 @@ def run_ours(args, cfg):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = torch.tensor([e0.elapsed_time(e1) / ne], dtype=torch.float64, device=dev)
-        if ws > 1:
-            dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
-        e2e = {"value": T * ws / (float(e_ms.item()) / 1e3), "unit": "queries/s", "h2d_bytes_per_step": h2d,
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / ne, ws, dev)
+        e2e = {"value": weak_scaling_value(T, ws, e_ms), "unit": "queries/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": ne}
         if dsa.dsa_get_device_error(sp) != 0:
             raise RuntimeError("device error during the end-to-end loop")
@@ -348,7 +359,7 @@ def run_ours(args, cfg):
         cpu = cpu_baseline(cfg, args)
     line = {
         "metric": METRIC,
-        "value": T * ws / (step_ms_max / 1e3),
+        "value": weak_scaling_value(T, ws, step_ms_max),
         "unit": "queries/s",
         "n_gpus": ws,
         "steps": args.steps,
