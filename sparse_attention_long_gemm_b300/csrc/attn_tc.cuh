@@ -532,6 +532,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (lane == 0) mbar_arrive_cluster(mapa(pr_free(b), peer));   // this warp's rows are read
             return true;
         };
+        // The output epilogue of a finished query is deferred until this lane has read S of the
+        // next query's first block (and, for peer lanes, sent its partial scores): the first
+        // exchange and Q.K^T of the next query then overlap the output stores.  The next query's
+        // first P.V (which overwrites O) needs P from every lane, given only after the epilogue.
+        int ep_r = -1, ep_gl = 0;
+        float ep_l = 1.f, ep_m = 0.f;
+        auto run_epilogue = [&]() -> bool {
+            if (ep_r < 0) return true;
+            if (!__all_sync(0xffffffffu, wait_bar(pv_done(ep_gl & 1), (ep_gl >> 1) & 1, timeout_ns, s_abort)))
+                return false;
+            tc_fence_after();
+            const float inv = 1.f / ep_l;
+            const long long orow = (static_cast<long long>(ep_r) * kAttnHeads + h) * kAttnDv + rank * 256;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 256; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(tmem_base + lane_off + C::TM_O + c0, o);
+                tmem_ld_wait();
+                uint4* dst = reinterpret_cast<uint4*>(out + orow + c0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(o[8 * q + 2 * e]) * inv,
+                                                                       __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+                        pk[e] = *reinterpret_cast<const uint32_t*>(&v);
+                    }
+                    dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
+            if (lse != nullptr && own)
+                lse[static_cast<long long>(ep_r) * kAttnHeads + h] = (ep_m + log2f(ep_l)) * 0.69314718055994530942f;
+            tc_fence_before();   // O has been read before the next query's first P.V overwrites it
+            ep_r = -1;
+            return true;
+        };
         while (r < rows && ok) {
             float m = -INFINITY, l = 0.f;             // own lanes: running max and denominator
             const int g0 = gi;
@@ -546,6 +583,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(s_free);                   // the next Q.K^T may overwrite S
+                if (i == 0 && own) {
+                    ok = run_epilogue();               // the previous query's output
+                    if (!ok) break;
+                }
                 if (!own) {
                     // ---- peer lanes: send this rank's partial scores of the peer's heads ----
                     ok = __all_sync(0xffffffffu, wait_bar<true>(xr_free(b), ((g >> 1) & 1) ^ 1, timeout_ns, s_abort));
@@ -563,9 +604,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         bulk_copy_to_peer(rX + b * C::XB, sbase + C::OFF_XS, C::XB, mapa(xr_full(b), peer));
                         bulk_pending = 1;
                     }
+                    if (i == 0) ok = run_epilogue();   // the previous query's output
                     // ---- then take the P of the PREVIOUS block from the peer, so that sending
                     // never waits for receiving ----
-                    if (i > 0) ok = take_p(g - 1, i - 1);
+                    if (ok && i > 0) ok = take_p(g - 1, i - 1);
                 } else {
                     // ---- own lanes: complete the scores, softmax, send P ----
                     if (hl == 0) mbar_expect_tx(xr_full(b), C::XB);
@@ -616,19 +658,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         l *= factor;
                         m = m_new;
                     }
-                    // P = 2^(z - m) in bf16 (pairs of keys per 32-bit column); l sums the rounded values
+                    // P = 2^(z - m) in bf16 (pairs of keys per 32-bit column); l sums the fp32 values
+                    // before rounding, in four independent partial sums
                     const float zs = pos_scale ? scale_log2 : 1.f;
                     uint32_t pk[32];
-                    float lsum = 0.f;
+                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const __nv_bfloat162 pr = __floats2bfloat162_rn(fast_exp2(fmaf(sv[2 * j], zs, -m)),
-                                                                        fast_exp2(fmaf(sv[2 * j + 1], zs, -m)));
-                        const float2 back = __bfloat1622float2(pr);
-                        lsum += back.x + back.y;
+                        const float p0 = fast_exp2(fmaf(sv[2 * j], zs, -m)), p1 = fast_exp2(fmaf(sv[2 * j + 1], zs, -m));
+                        const __nv_bfloat162 pr = __floats2bfloat162_rn(p0, p1);
+                        ls[j & 3] += p0 + p1;
                         pk[j] = *reinterpret_cast<const uint32_t*>(&pr);
                     }
-                    l += lsum;
+                    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster_relaxed(mapa(xr_free(b), peer));   // this warp's rows are read
                     // send P, the rescale factor and the denominator to the peer
@@ -686,35 +728,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ok = take_q(rp);
                 rp += 2;
             }
-            // ---------------- epilogue of the finished query ----------------
-            const int gl = gi - 1;
-            ok = ok && __all_sync(0xffffffffu, wait_bar(pv_done(gl & 1), (gl >> 1) & 1, timeout_ns, s_abort));
+            // ---------------- epilogue of the finished query: deferred (see run_epilogue) ----------------
+            ep_r = r_cur;
+            ep_gl = gi - 1;
+            ep_l = l_fin;
+            ep_m = m_fin;
             if (!ok) break;
-            tc_fence_after();
-            const float inv = 1.f / l_fin;
-            const long long orow = (static_cast<long long>(r_cur) * kAttnHeads + h) * kAttnDv + rank * 256;
-#pragma unroll 1
-            for (int c0 = 0; c0 < 256; c0 += 32) {
-                uint32_t o[32];
-                tmem_ld32(tmem_base + lane_off + C::TM_O + c0, o);
-                tmem_ld_wait();
-                uint4* dst = reinterpret_cast<uint4*>(out + orow + c0);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(o[8 * q + 2 * e]) * inv,
-                                                                       __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
-                        pk[e] = *reinterpret_cast<const uint32_t*>(&v);
-                    }
-                    dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
-            }
-            if (lse != nullptr && own)
-                lse[static_cast<long long>(r_cur) * kAttnHeads + h] = (m_fin + log2f(l_fin)) * 0.69314718055994530942f;
-            tc_fence_before();   // O has been read before the next query's first P.V overwrites it
         }
+        if (ok) ok = run_epilogue();                  // the last query's output
         if (bulk_pending) bulk_wait_read();
         (void)qi;
     }
