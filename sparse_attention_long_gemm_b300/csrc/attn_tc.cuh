@@ -18,20 +18,22 @@
 // owns heads 64r .. 64r+63.  Per 64-key block each rank sends the peer its
 // partial scores of the peer's heads (16 KB, fp32) and receives the peer's
 // partial scores of its own heads; it completes S = S_0 + S_1 for its heads,
-// runs their online softmax, and sends the peer their probabilities P (bf16)
-// together with each head's O rescale factor (and, for the final block, the
-// softmax denominators).  Both ranks then hold P for all 128 heads and
-// accumulate O[:, their 256 latent columns] += P . V_r.  No flop is
-// duplicated, and 24.5 KB per block cross between the CTAs in each
-// direction (distributed shared memory moves ~14.5 B/clk per SM, so these
-// bytes, not the tensor cores, would otherwise set the pace).
+// runs their online softmax, and writes their probabilities P (bf16) straight
+// into its half of a 128-head P tile in shared memory, the A operand of P.V.
+// The same 8 KB half is bulk-copied into the peer's P tile, together with each
+// head's O rescale factor and softmax denominator (512 B).  Both ranks then
+// hold P for all 128 heads and accumulate O[:, their 256 latent columns] +=
+// P . V_r.  No flop is duplicated, and 24.5 KB per block cross between the
+// CTAs in each direction (distributed shared memory moves ~14.5 B/clk per SM).
 //
 // Tensor memory of a CTA (512 columns x 128 lanes, lane = head):
 //   [0, 256)    O_r, fp32 accumulator
 //   [256, 384)  Q_r latent part, bf16 pairs: the A operand of Q.K^T
-//   [384, 448)  S: fp32 partial scores of the current 64-key block (single:
-//               the next Q.K^T starts as soon as every lane has read it)
-//   [448, 512)  P buffers 0 and 1: bf16 probabilities, the A operand of P.V
+//   [384, 512)  S buffers 0 and 1: fp32 partial scores of a 64-key block.
+//               Two buffers let the tensor cores run the Q.K^T of later
+//               blocks while the softmax of the current one waits for the
+//               exchange, so the exchange of a block overlaps the softmax of
+//               the block before it.
 //
 // Shared memory is mostly a 4-slot ring.  Its items, in the order every role
 // walks them: per query, one Q item (two slots: the latent part of Q_r in
@@ -42,8 +44,9 @@
 // and a small rope buffer, freeing its slots at once, so nearly the whole ring
 // holds gathers in flight: random rows reach about 9 TB/s from L2 only with
 // ~100 KB per SM in flight and with requests of 512 contiguous bytes.  The
-// rest holds the exchange buffers (received tiles double-buffered, outgoing
-// tiles staged once and sent by one bulk copy each).
+// rest holds the two P tiles (128B-swizzled, K-major), the received partial
+// scores (one tile), the outgoing partial scores (staged once and sent by one
+// bulk copy) and the rescale factors / denominators (two buffers each way).
 //
 // Per CTA (256 threads; the warp of a role depends on the rank so that the two
 // warps running the softmax have their SM sub-partitions to themselves):
@@ -51,16 +54,23 @@
 //               warps whose lanes are this rank's heads ("own" warps)
 //               complete their scores, run the online softmax (running max
 //               updated lazily: O is rescaled only when it grows by more than
-//               2^8) and send P; the two others ("peer" warps) send their
-//               lanes' partial scores and move the P received for those
-//               heads into tensor memory, rescaling those O rows first when
-//               told to.  All four move Q items into tensor memory and run
-//               the output epilogue;
+//               2^8) and write their half of the P tile; the two others
+//               ("peer" warps) send their lanes' partial scores, take the
+//               rescale factors that come with the peer's half of P
+//               (rescaling those O rows first when told to), and hand that
+//               half of the tile back to the peer once its P.V has completed.
+//               All four move Q items into tensor memory and run the output
+//               epilogue;
+//   one warp    copy warp (warp 4 on rank 0, warp 6 on rank 1): one thread
+//               sends this rank's half of each P tile, with its factors, to
+//               the peer by bulk copy as soon as the own warps have written
+//               it and the peer has freed its copy, so the own warps never
+//               wait for the peer;
 //   one warp    TMEM allocation and tcgen05.mma issue (one thread, polling
 //               both the next Q.K^T and the next P.V so neither waits on the
 //               other): warp 6 on rank 0, warp 4 on rank 1;
-//   one warp    producer (warp 7 on rank 0, warp 5 on rank 1; the other two
-//               warps of 4..7 are idle): the rows of a KV item by cp.async, each warp
+//   one warp    producer (warp 7 on rank 0, warp 5 on rank 1; the fourth
+//               warp of 4..7 is idle): the rows of a KV item by cp.async, each warp
 //               instruction one key's 512 latent bytes (the rope parts of 8
 //               keys per instruction), completion signalled with
 //               cp.async.mbarrier.arrive.noinc so the producers never wait for
@@ -90,32 +100,36 @@ struct AttnTc {
     static constexpr int QR_HALF = 64 * 64;                         // 64 heads x 32 rope cols = 4 KB
     static constexpr int QR_BYTES = 2 * QR_HALF;
     static constexpr int XB = 64 * kAttnBK * 4;                     // partial scores of 64 heads: 16 KB
-    static constexpr int PB_P = 64 * kAttnBK * 2;                   // P of 64 heads: 8 KB
-    static constexpr int PB = PB_P + 64 * 4 + 64 * 4;               // + rescale factors + denominators
+    static constexpr int PT = kAttnHeads * kAttnBK * 2;             // P tile of 128 heads: 16 KB
+    static constexpr int PH = PT / 2;                               // one rank's 64 heads of it
+    static constexpr int MB = 64 * 4 * 2;                           // rescale factors + denominators
     static constexpr int OFF_RING = 0;
     static constexpr int OFF_QR = OFF_RING + kAttnSlots * SLOT;
-    static constexpr int OFF_XR = OFF_QR + QR_BYTES;                // [2] received partial scores
-    static constexpr int OFF_XS = OFF_XR + 2 * XB;                  // outgoing partial scores
-    static constexpr int OFF_PR = OFF_XS + XB;                      // [2] received P message
-    static constexpr int OFF_PS = OFF_PR + 2 * PB;                  // outgoing P message
-    static constexpr int OFF_BAR = OFF_PS + PB;
-    // full[S], empty[S], q_tm_full, s_full, s_free, p_full[2], pv_done[2],
-    // xr_full[2], xr_free[2], pr_full[2], pr_free[2], done
-    static constexpr int NBAR = 2 * kAttnSlots + 1 + 1 + 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1;
+    static constexpr int OFF_P = OFF_QR + QR_BYTES;                 // [2] P tiles
+    static constexpr int OFF_XR = OFF_P + 2 * PT;                   // received partial scores
+    static constexpr int OFF_XS = OFF_XR + XB;                      // outgoing partial scores
+    static constexpr int OFF_MR = OFF_XS + XB;                      // [2] received factors / denominators
+    static constexpr int OFF_MS = OFF_MR + 2 * MB;                  // [2] outgoing factors / denominators
+    static constexpr int OFF_BAR = OFF_MS + 2 * MB;
+    // full[S], empty[S], q_tm_full, s_full[2], s_free[2], p_full[2], pv_done[2],
+    // xr_full, xr_free, pr_full[2], pr_free[2], done, p_ready[2], pcopy_done[2]
+    static constexpr int NBAR = 2 * kAttnSlots + 1 + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 2 + 1 + 2 + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;               // + alignment slack
     static constexpr int TMEM_COLS = 512;
     static constexpr int TM_O = 0;
     static constexpr int TM_Q = 256;
-    static constexpr int TM_S = 384;
-    static constexpr int TM_P = 448;      // + 32 * buffer
+    static constexpr int TM_S = 384;      // + 64 * buffer
     static constexpr uint32_t IDESC_QK = idesc_bf16(128, kAttnBK, false, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
     static constexpr uint32_t Q_TX = 4 * QL_TILE + QR_BYTES;
+    static constexpr uint32_t P_TX = PH + MB;                       // bytes of one P message
 };
 static_assert(AttnTc::SMEM <= 232448, "attention shared memory exceeds the per-CTA limit");
+static_assert(AttnTc::OFF_P % 1024 == 0, "the P tiles are 128B-swizzled operands (1024-byte atoms)");
 static_assert(2 * AttnTc::QL_TILE + AttnTc::QR_HALF <= AttnTc::SLOT, "a Q item must fit in two slots");
-static_assert(AttnTc::PB % 16 == 0 && AttnTc::XB % 16 == 0, "bulk copies move multiples of 16 bytes");
+static_assert(AttnTc::PH % 16 == 0 && AttnTc::MB % 16 == 0 && AttnTc::XB % 16 == 0,
+              "bulk copies move multiples of 16 bytes");
 
 // Shared-memory matrix descriptor, 64-byte-swizzled K-major operand
 // (rows of 64 B, 8-row atoms of 512 B).
@@ -142,14 +156,17 @@ __device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
 
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into
 // another CTA's (address from mapa); completes `bytes` on that CTA's mbarrier.
-// Tracked in this thread's bulk async-group for bulk_wait_read().
+// bulk_commit() closes this thread's current bulk async-group.
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t rdst, uint32_t src, uint32_t bytes, uint32_t rbar) {
     asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(rdst), "r"(src), "r"(bytes), "r"(rbar) : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// Waits until every bulk copy committed by this thread has finished reading its source.
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's most recent bulk async-groups still read their sources.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 
 // Arrive on `bar` once every cp.async issued so far by this thread has landed
 // (the arrival counts against the barrier's expected count).
@@ -157,10 +174,17 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Arrive on an mbarrier of the peer CTA without release semantics.  Used where
-// the only accesses to order are this thread's earlier shared-memory loads of
-// the buffer being released, whose values have already been consumed by
-// instructions before the arrive (so the loads have completed).
+// Arrive on an mbarrier of the peer CTA without release semantics, once the
+// shared-memory loads that produced `dep` have returned their data: `dep` (any
+// bits of the loaded values, combined by the caller) is folded into the
+// address through an opaque zeroing step, so the arrive cannot issue before
+// those loads complete.  Used to hand back a receive buffer whose contents
+// this warp has read into registers; nothing written before needs ordering.
+__device__ __forceinline__ void mbar_arrive_cluster_after(uint32_t remote_bar, uint32_t dep) {
+    asm volatile("and.b32 %0, %0, 0;" : "+r"(dep));
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar + dep) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
@@ -193,15 +217,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     auto full = [&](int i) { return bar0 + 8u * i; };
     auto empty = [&](int i) { return bar0 + 8u * (kAttnSlots + i); };
     const uint32_t q_tm_full = bar0 + 8u * (2 * kAttnSlots);
-    const uint32_t s_full = bar0 + 8u * (2 * kAttnSlots + 1);
-    const uint32_t s_free = bar0 + 8u * (2 * kAttnSlots + 2);
-    auto p_full = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 3 + i); };
-    auto pv_done = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 5 + i); };
-    auto xr_full = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 7 + i); };
-    auto xr_free = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 9 + i); };
+    auto s_full = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 1 + i); };
+    auto s_free = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 3 + i); };
+    auto p_full = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 5 + i); };
+    auto pv_done = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 7 + i); };
+    const uint32_t xr_full = bar0 + 8u * (2 * kAttnSlots + 9);
+    const uint32_t xr_free = bar0 + 8u * (2 * kAttnSlots + 10);
     auto pr_full = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 11 + i); };
     auto pr_free = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 13 + i); };
     const uint32_t done_bar = bar0 + 8u * (2 * kAttnSlots + 15);
+    auto p_ready = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 16 + i); };
+    auto pcopy_done = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 18 + i); };
+    const uint32_t sP = sbase + C::OFF_P;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     auto slot_addr = [&](int rp) { return sRing + static_cast<uint32_t>(rp % kAttnSlots) * C::SLOT; };
@@ -214,20 +241,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // and 2,3 on rank 1, so the MMA and producer warps go to the other two sub-partitions.
     const int mma_warp = (rank == 0) ? 6 : 4;
     const int prod_warp = (rank == 0) ? 7 : 5;
+    const int copy_warp = (rank == 0) ? 4 : 6;
 
     if (tid == 0) {
         for (int i = 0; i < kAttnSlots; ++i) { mbar_init(full(i), kAttnProducers); mbar_init(empty(i), 1); }
         mbar_init(q_tm_full, 128);
-        mbar_init(s_full, 1);
-        mbar_init(s_free, 128);
         for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full(i), 1);
+            mbar_init(s_free(i), 128);
             mbar_init(p_full(i), 128);
             mbar_init(pv_done(i), 1);
-            mbar_init(xr_full(i), 1);     // a local expect_tx; the peer's bulk copy completes it
-            mbar_init(xr_free(i), 2);     // one arrive per own warp of the peer
-            mbar_init(pr_full(i), 1);
-            mbar_init(pr_free(i), 2);     // one arrive per peer warp of the peer
+            mbar_init(pr_full(i), 1);     // a local expect_tx; the peer's bulk copies complete it
+            mbar_init(pr_free(i), 1);     // one arrive from the peer once its P.V of the buffer is done
+            mbar_init(p_ready(i), 2);     // one arrive per own warp: its rows of P and factors are written
+            mbar_init(pcopy_done(i), 1);  // the copy warp: this rank's half has been read by its copy
         }
+        mbar_init(xr_full, 1);            // a local expect_tx; the peer's bulk copy completes it
+        mbar_init(xr_free, 2);            // one arrive per own warp of the peer
         mbar_init(done_bar, 1);
         *s_abort = 0;
         fence_mbar_init();
@@ -335,11 +365,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             auto dK = [&](int rp_) { return sdesc_sw128(slot_addr(rp_), 16, 1024); };
             auto dR = [&](int rp_) { return sdesc_sw64(slot_addr(rp_) + 4 * C::KV_SLOT); };
             auto dV = [&](int rp_) { return sdesc_sw128(slot_addr(rp_), C::KV_SLOT, 1024); };
-            auto issue_qk = [&](int rp_) -> bool {
-                if (!wait_bar(full(rp_ % kAttnSlots), (rp_ / kAttnSlots) & 1, timeout_ns, s_abort)) return false;
+            // Q.K^T of block g into S buffer g & 1 (its KV item is in ring position rp_)
+            auto issue_qk = [&](int g, int rp_) {
                 fence_proxy_async_smem();   // rows written by cp.async, read by the tensor cores
                 tc_fence_after();
-                const uint32_t d = tmem_base + C::TM_S;
+                const uint32_t d = tmem_base + C::TM_S + static_cast<uint32_t>(g & 1) * kAttnBK;
                 const uint64_t bk = dK(rp_), br = dR(rp_);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -353,17 +383,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int kk = 0; kk < 2; ++kk)
                     tc_mma_bf16(d, dQR + static_cast<uint64_t>(kk * 2), br + static_cast<uint64_t>(kk * 2),
                                 C::IDESC_QK, 1u);
-                tc_commit(s_full);
-                return true;
+                tc_commit(s_full(g & 1));
             };
+            // O += P . V of block g: P from P tile g & 1 (K-major, 128B-swizzled rows of 64 keys)
             auto issue_pv = [&](int g, int rp_, bool first) {
                 const uint64_t bv = dV(rp_);
+                const uint64_t bp = sdesc_sw128(sP + static_cast<uint32_t>(g & 1) * C::PT, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kAttnBK / 16; ++kk)
                     // V (MN-major): the 4 latent slots are the 64-column chunks (LBO), 8-key groups 1 KB apart
-                    tc_mma_bf16_ts(tmem_base + C::TM_O, tmem_base + C::TM_P + (g & 1) * 32 + kk * 8,
-                                   bv + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::IDESC_PV,
-                                   (!first || kk) ? 1u : 0u);
+                    tc_mma_bf16(tmem_base + C::TM_O, bp + static_cast<uint64_t>(kk * 2),
+                                bv + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::IDESC_PV,
+                                (!first || kk) ? 1u : 0u);
                 tc_commit(pv_done(g & 1));
                 tc_commit(empty(rp_ % kAttnSlots));
             };
@@ -375,20 +406,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (!ok) break;
                 tc_fence_after();
                 const int g0 = gi, rp0 = rp, gend = gi + A.nb;
-                ok = issue_qk(rp0);
-                // Q.K^T of block j needs S free (block j-1 read by every lane); P.V of block j
-                // needs its P.  Issue whichever is ready, in block order within each kind.
-                int qk_next = g0 + 1, pv_next = g0;
+                // Q.K^T of block j needs its KV item and S buffer j & 1 free (block j-2 read by
+                // every lane); P.V of block j needs both halves of its P tile.  Issue whichever is
+                // ready, in block order within each kind.
+                int qk_next = g0, pv_next = g0;
                 uint64_t t_idle = 0;
                 while (ok && pv_next < gend) {
                     bool progressed = false;
-                    if (qk_next < gend && mbar_try(s_free, (qk_next - 1) & 1)) {
-                        tc_fence_after();
-                        ok = issue_qk(rp0 + (qk_next - g0));
-                        ++qk_next;
-                        progressed = true;
+                    if (qk_next < gend) {
+                        const int rq = rp0 + (qk_next - g0);
+                        if (mbar_try(s_free(qk_next & 1), ((qk_next >> 1) & 1) ^ 1) &&
+                            mbar_try(full(rq % kAttnSlots), (rq / kAttnSlots) & 1)) {
+                            issue_qk(qk_next, rq);
+                            ++qk_next;
+                            progressed = true;
+                        }
                     }
-                    if (ok && pv_next < qk_next && mbar_try(p_full(pv_next & 1), (pv_next >> 1) & 1)) {
+                    if (pv_next < qk_next && mbar_try(p_full(pv_next & 1), (pv_next >> 1) & 1) &&
+                        mbar_try_cluster(pr_full(pv_next & 1), (pv_next >> 1) & 1)) {
                         tc_fence_after();
                         issue_pv(pv_next, rp0 + (pv_next - g0), pv_next == g0);
                         ++pv_next;
@@ -415,6 +450,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             tc_commit(done_bar);                          // every MMA issued has completed
             wait_bar(done_bar, 0, timeout_ns, nullptr);   // before TMEM is released
+        }
+    } else if (warp == copy_warp) {
+        // ---------------- copy warp: sends this rank's half of each P tile to the peer ----------------
+        if (lane == 0) {
+            const uint32_t rP = mapa(sP, peer), rMR = mapa(sbase + C::OFF_MR, peer);
+            int g = 0;
+            bool ok = true;
+            for (int r = cl; r < rows && ok; r += ncl) {
+                const AttnRow A = attn_row(rs, r, k);
+                for (int i = 0; i < A.nb && ok; ++i, ++g) {
+                    const int b = g & 1;
+                    // the own warps have written the rows; the peer's P.V of block g-2 has completed
+                    ok = wait_bar(p_ready(b), (g >> 1) & 1, timeout_ns, s_abort) &&
+                         wait_bar<true>(pr_free(b), ((g >> 1) & 1) ^ 1, timeout_ns, s_abort);
+                    if (!ok) break;
+                    const uint32_t rb = mapa(pr_full(b), peer);
+                    const uint32_t off = static_cast<uint32_t>(b * C::PT + rank * C::PH);
+                    bulk_copy_to_peer(rP + off, sP + off, C::PH, rb);
+                    bulk_copy_to_peer(rMR + b * C::MB, sbase + C::OFF_MS + b * C::MB, C::MB, rb);
+                    bulk_commit();
+                    bulk_wait_read<0>();
+                    mbar_arrive(pcopy_done(b));
+                }
+            }
+            bulk_wait_read<0>();
         }
     } else if (warp < 4) {
         // ---------------- softmax group / Q items / epilogue (warps 0..3) ----------------
@@ -498,39 +558,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ok = take_q(rp);
             rp += 2;
         }
-        const uint32_t rX = mapa(sbase + C::OFF_XR, peer), rP = mapa(sbase + C::OFF_PR, peer);
+        const uint32_t rXR = mapa(sbase + C::OFF_XR, peer);
         float l_peer = 1.f;                           // peer lanes: the denominator received last
-        // Peer lanes: takes the P of block g (the i-th of the query) that the peer computed for
-        // these heads, rescales these O rows if told to, and hands P to the tensor cores.
+        // Peer lanes: takes the rescale factors and denominators that came with the peer's half of
+        // P tile g & 1 (block g, the i-th of the query), rescales these O rows if told to, and
+        // releases the P.V of block g.  Then hands the peer back its half of the tile of block
+        // g - 1 once that block's P.V has completed.
         auto take_p = [&](int g, int i) -> bool {
             const int b = g & 1;
-            if (hl == 0) mbar_expect_tx(pr_full(b), C::PB);
+            if (hl == 0) mbar_expect_tx(pr_full(b), C::P_TX);
             if (!__all_sync(0xffffffffu, wait_bar<true>(pr_full(b), (g >> 1) & 1, timeout_ns, s_abort))) return false;
-            const uint8_t* pm = smem + C::OFF_PR + b * C::PB;
-            const float f = reinterpret_cast<const float*>(pm + C::PB_P)[hl];
-            l_peer = reinterpret_cast<const float*>(pm + C::PB_P + 256)[hl];
-            uint32_t pk[32];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 u = *reinterpret_cast<const uint4*>(pm + hl * 128 + (((c ^ hl) & 7) << 4));
-                pk[4 * c + 0] = u.x; pk[4 * c + 1] = u.y; pk[4 * c + 2] = u.z; pk[4 * c + 3] = u.w;
-            }
+            const float* mr = reinterpret_cast<const float*>(smem + C::OFF_MR + b * C::MB);
+            const float f = mr[hl];
+            l_peer = mr[64 + hl];
             if (i > 0 && __any_sync(0xffffffffu, f != 1.f)) {
                 // O must hold every earlier P.V before it is rescaled
                 if (!__all_sync(0xffffffffu, wait_bar(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, timeout_ns, s_abort)))
                     return false;
                 tc_fence_after();
                 rescale_o(f);
+                tmem_st_wait();
             }
-            if (!wait_p_buffer(g)) return false;
-            tc_fence_after();
-            tmem_st32(tmem_base + lane_off + C::TM_P + b * 32, pk);
-            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(p_full(b));
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa(pr_free(b), peer));   // this warp's rows are read
-            return true;
+            // The tile half and factors of block g - 1 were last read by that block's P.V (its
+            // completion is observed here) and by this warp's loads, consumed long before.
+            bool w = true;
+            if (g > 0 && hl == 0) {
+                w = wait_bar(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, timeout_ns, s_abort);
+                if (w) mbar_arrive_cluster_relaxed(mapa(pr_free((g - 1) & 1), peer));
+            }
+            return __all_sync(0xffffffffu, w);
         };
         // The output epilogue of a finished query is deferred until this lane has read S of the
         // next query's first block (and, for peer lanes, sent its partial scores): the first
@@ -574,24 +632,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const int g0 = gi;
             for (int i = 0; i < A.nb && ok; ++i) {
                 const int g = g0 + i, b = g & 1;
-                ok = __all_sync(0xffffffffu, wait_bar(s_full, g & 1, timeout_ns, s_abort));
+                ok = __all_sync(0xffffffffu, wait_bar(s_full(b), (g >> 1) & 1, timeout_ns, s_abort));
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t sraw[64];
-                tmem_ld32(tmem_base + lane_off + C::TM_S, *reinterpret_cast<uint32_t(*)[32]>(sraw));
-                tmem_ld32(tmem_base + lane_off + C::TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(sraw + 32));
+                const uint32_t ts = tmem_base + lane_off + C::TM_S + static_cast<uint32_t>(b) * kAttnBK;
+                tmem_ld32(ts, *reinterpret_cast<uint32_t(*)[32]>(sraw));
+                tmem_ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(sraw + 32));
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(s_free);                   // the next Q.K^T may overwrite S
-                if (i == 0 && own) {
-                    ok = run_epilogue();               // the previous query's output
-                    if (!ok) break;
-                }
+                mbar_arrive(s_free(b));                // Q.K^T of block g + 2 may overwrite this buffer
                 if (!own) {
                     // ---- peer lanes: send this rank's partial scores of the peer's heads ----
-                    ok = __all_sync(0xffffffffu, wait_bar<true>(xr_free(b), ((g >> 1) & 1) ^ 1, timeout_ns, s_abort));
-                    if (!ok) break;
-                    if (bulk_pending) bulk_wait_read();  // the previous tile has left XS
+                    if (bulk_pending) bulk_wait_read<0>();   // the previous tile has left XS
                     named_sync(2, 64);
                     uint8_t* xs = smem + C::OFF_XS + hl * 256;
 #pragma unroll
@@ -600,29 +653,49 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             make_uint4(sraw[4 * c], sraw[4 * c + 1], sraw[4 * c + 2], sraw[4 * c + 3]);
                     fence_proxy_async_smem();
                     named_sync(2, 64);
+                    bool sent = true;
                     if (hl == 0) {
-                        bulk_copy_to_peer(rX + b * C::XB, sbase + C::OFF_XS, C::XB, mapa(xr_full(b), peer));
-                        bulk_pending = 1;
+                        // the peer has read the previous block's partial scores out of its XR
+                        sent = wait_bar<true>(xr_free, (g & 1) ^ 1, timeout_ns, s_abort);
+                        if (sent) {
+                            bulk_copy_to_peer(rXR, sbase + C::OFF_XS, C::XB, mapa(xr_full, peer));
+                            bulk_commit();
+                            bulk_pending = 1;
+                        }
                     }
-                    if (i == 0) ok = run_epilogue();   // the previous query's output
-                    // ---- then take the P of the PREVIOUS block from the peer, so that sending
-                    // never waits for receiving ----
+                    ok = __all_sync(0xffffffffu, sent);
+                    if (ok && i == 0) ok = run_epilogue();   // the previous query's output
+                    // ---- then take the peer's P of the PREVIOUS block, so that sending never
+                    // waits for receiving ----
                     if (ok && i > 0) ok = take_p(g - 1, i - 1);
                 } else {
-                    // ---- own lanes: complete the scores, softmax, send P ----
-                    if (hl == 0) mbar_expect_tx(xr_full(b), C::XB);
-                    ok = __all_sync(0xffffffffu, wait_bar<true>(xr_full(b), (g >> 1) & 1, timeout_ns, s_abort));
+                    // ---- own lanes: complete the scores, softmax, write P for both ranks ----
+                    if (i == 0) {
+                        ok = run_epilogue();           // the previous query's output
+                        if (!ok) break;
+                    }
+                    // this rank's half of P tile b and factor buffer b are free once the P.V of block
+                    // g-2 has completed here and their copy to the peer has been read
+                    ok = wait_p_buffer(g) &&
+                         __all_sync(0xffffffffu, wait_bar(pcopy_done(b), ((g >> 1) & 1) ^ 1, timeout_ns, s_abort));
+                    if (!ok) break;
+                    if (hl == 0) mbar_expect_tx(xr_full, C::XB);
+                    ok = __all_sync(0xffffffffu, wait_bar<true>(xr_full, g & 1, timeout_ns, s_abort));
                     if (!ok) break;
                     float sv[64];
-                    const uint8_t* xr = smem + C::OFF_XR + b * C::XB + hl * 256;
+                    const uint8_t* xr = smem + C::OFF_XR + hl * 256;
+                    uint32_t dep = 0;
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
                         const float4 v = *reinterpret_cast<const float4*>(xr + (((c ^ hl) & 15) << 4));
+                        dep |= __float_as_uint(v.x);
                         sv[4 * c + 0] = __uint_as_float(sraw[4 * c + 0]) + v.x;
                         sv[4 * c + 1] = __uint_as_float(sraw[4 * c + 1]) + v.y;
                         sv[4 * c + 2] = __uint_as_float(sraw[4 * c + 2]) + v.z;
                         sv[4 * c + 3] = __uint_as_float(sraw[4 * c + 3]) + v.w;
                     }
+                    // this warp's rows of XR are in registers (each warp load completes for all lanes)
+                    if (lane == 0) mbar_arrive_cluster_after(mapa(xr_free, peer), dep);
                     // columns past the last valid entry are masked (identical for every head)
                     const int nvalid = A.nsel - i * kAttnBK;
                     if (nvalid < kAttnBK) {
@@ -671,38 +744,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         pk[j] = *reinterpret_cast<const uint32_t*>(&pr);
                     }
                     l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster_relaxed(mapa(xr_free(b), peer));   // this warp's rows are read
-                    // send P, the rescale factor and the denominator to the peer
-                    ok = __all_sync(0xffffffffu, wait_bar<true>(pr_free(b), ((g >> 1) & 1) ^ 1, timeout_ns, s_abort));
-                    if (!ok) break;
-                    if (bulk_pending) bulk_wait_read();  // the previous message has left PS
-                    named_sync(3, 64);
-                    uint8_t* ps = smem + C::OFF_PS;
+                    uint8_t* pt = smem + C::OFF_P + b * C::PT + h * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(ps + hl * 128 + (((c ^ hl) & 7) << 4)) =
+                        *reinterpret_cast<uint4*>(pt + (((c ^ h) & 7) << 4)) =
                             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                    reinterpret_cast<float*>(ps + C::PB_P)[hl] = factor;
-                    reinterpret_cast<float*>(ps + C::PB_P + 256)[hl] = l;
+                    float* ms = reinterpret_cast<float*>(smem + C::OFF_MS + b * C::MB);
+                    ms[hl] = factor;
+                    ms[64 + hl] = l;
                     fence_proxy_async_smem();
-                    named_sync(3, 64);
-                    if (hl == 0) {
-                        bulk_copy_to_peer(rP + b * C::PB, sbase + C::OFF_PS, C::PB, mapa(pr_full(b), peer));
-                        bulk_pending = 1;
-                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_ready(b));   // the copy warp sends these rows to the peer
                     if (i > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
                         ok = __all_sync(0xffffffffu,
                                         wait_bar(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, timeout_ns, s_abort));
                         if (!ok) break;
                         tc_fence_after();
                         rescale_o(factor);
+                        tmem_st_wait();
                     }
-                    ok = wait_p_buffer(g);
-                    if (!ok) break;
-                    tc_fence_after();
-                    tmem_st32(tmem_base + lane_off + C::TM_P + b * 32, pk);
-                    tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(p_full(b));
                 }
@@ -736,7 +796,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (!ok) break;
         }
         if (ok) ok = run_epilogue();                  // the last query's output
-        if (bulk_pending) bulk_wait_read();
+        if (bulk_pending) bulk_wait_read<0>();
         (void)qi;
     }
 
