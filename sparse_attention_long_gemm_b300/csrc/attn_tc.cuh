@@ -69,10 +69,10 @@
 //   one warp    TMEM allocation and tcgen05.mma issue (one thread, polling
 //               both the next Q.K^T and the next P.V so neither waits on the
 //               other): warp 6 on rank 0, warp 4 on rank 1;
-//   one warp    producer (warp 7 on rank 0, warp 5 on rank 1; the fourth
-//               warp of 4..7 is idle): the rows of a KV item by cp.async, each warp
-//               instruction one key's 512 latent bytes (the rope parts of 8
-//               keys per instruction), completion signalled with
+//   two warps   producers (warps 5 and 7), each
+//               gathering half of the keys of every KV item by cp.async: each
+//               warp instruction one key's 512 latent bytes (the rope parts of
+//               8 keys per instruction), completion signalled with
 //               cp.async.mbarrier.arrive.noinc so the producers never wait for
 //               data; index loads run four blocks ahead; one thread issues the
 //               TMA loads of Q items.
@@ -90,7 +90,7 @@ constexpr int kAttnDv = 512;
 constexpr int kAttnBK = 64;              // selected keys per block
 constexpr int kAttnSlots = 4;            // ring slots
 constexpr int kAttnThreads = 256;
-constexpr int kAttnProducers = 32;       // threads of the producer warp
+constexpr int kAttnProducers = 64;       // threads of the two producer warps
 
 struct AttnTc {
     static constexpr int KV_SLOT = kAttnBK * 128;                   // 64 keys x 64 latent cols = 8 KB
@@ -242,6 +242,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int mma_warp = (rank == 0) ? 6 : 4;
     const int prod_warp = (rank == 0) ? 7 : 5;
     const int copy_warp = (rank == 0) ? 4 : 6;
+    const int prod_warp2 = (rank == 0) ? 5 : 7;
 
     if (tid == 0) {
         for (int i = 0; i < kAttnSlots; ++i) { mbar_init(full(i), kAttnProducers); mbar_init(empty(i), 1); }
@@ -274,9 +275,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == prod_warp) {
-        // ---------------- producer: Q items (TMA) and KV items (cp.async) ----------------
-        const int pt = lane;
+    if (warp == prod_warp || warp == prod_warp2) {
+        // ---------------- producers: Q items (TMA) and KV items (cp.async) ----------------
+        // Each warp gathers half of every block's keys (keys 32 pw .. 32 pw + 31).
+        const int pw = (warp == prod_warp) ? 0 : 1;
         int rp = 0;
         bool ok = true;
         for (int r = cl; r < rows && ok; r += ncl) {
@@ -286,7 +288,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ok = wait_bar(empty(rp % kAttnSlots), ((rp / kAttnSlots) & 1) ^ 1, timeout_ns, s_abort) &&
                  wait_bar(empty((rp + 1) % kAttnSlots), (((rp + 1) / kAttnSlots) & 1) ^ 1, timeout_ns, s_abort);
             if (!ok) break;
-            if (pt == 0) {
+            if (pw == 0 && lane == 0) {
                 const uint32_t fb = full(rp % kAttnSlots);
                 mbar_expect_tx(fb, C::Q_TX);
                 for (int j = 0; j < 4; ++j)
@@ -303,50 +305,39 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // KV items
             const int* irow = idx + static_cast<long long>(r) * k;
             const long long kb = A.ri.key_base;
-            // lane l loads the indices of keys l and l+32 of each block, four blocks ahead
-            int e0[2], e1[2], e2[2], e3[2];
-            auto ld_ent = [&](int i, int (&v)[2]) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int ent = i * kAttnBK + hh * 32 + lane;
-                    v[hh] = (ent < A.nsel) ? __ldg(irow + ent) : 0;
-                }
+            // lane l loads the index of key 32 pw + l of each block, four blocks ahead
+            auto ld_ent = [&](int i) -> int {
+                const int ent = i * kAttnBK + pw * 32 + lane;
+                return (ent < A.nsel) ? __ldg(irow + ent) : 0;
             };
-            ld_ent(0, e0); ld_ent(1, e1); ld_ent(2, e2); ld_ent(3, e3);
+            int e0 = ld_ent(0), e1 = ld_ent(1), e2 = ld_ent(2), e3 = ld_ent(3);
             for (int i = 0; i < A.nb && ok; ++i, ++rp) {
-                long long myrow[2];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    int s = e0[hh];
-                    if (s < 0 || s >= A.ri.n) {
-                        if (i * kAttnBK + hh * 32 + lane < A.nsel) raise_error(DSA_ERR_DEVICE_DATA);
-                        s = 0;   // any in-range row; entries past nsel are masked by the softmax
-                    }
-                    myrow[hh] = kb + s;
-                    e0[hh] = e1[hh]; e1[hh] = e2[hh]; e2[hh] = e3[hh];
+                int s_ = e0;
+                if (s_ < 0 || s_ >= A.ri.n) {
+                    if (i * kAttnBK + pw * 32 + lane < A.nsel) raise_error(DSA_ERR_DEVICE_DATA);
+                    s_ = 0;   // any in-range row; entries past nsel are masked by the softmax
                 }
-                ld_ent(i + 4, e3);
+                const long long myrow = kb + s_;
+                e0 = e1; e1 = e2; e2 = e3;
+                e3 = ld_ent(i + 4);
                 ok = wait_bar(empty(rp % kAttnSlots), ((rp / kAttnSlots) & 1) ^ 1, timeout_ns, s_abort);
                 if (!ok) break;
                 const uint32_t st = slot_addr(rp);
                 // latent: one key (512 contiguous bytes) per warp instruction
                 const int j = lane >> 3, c = lane & 7;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll 8
-                    for (int kk = 0; kk < 32; ++kk) {
-                        const long long row = __shfl_sync(0xffffffffu, myrow[hh], kk);
-                        const int key = hh * 32 + kk;
-                        cp_async_16(st + j * C::KV_SLOT + key * 128 + (((c ^ key) & 7) << 4),
-                                    kv + row * kAttnDqk + rank * 256 + lane * 8);
-                    }
+                for (int kk = 0; kk < 32; ++kk) {
+                    const long long row = __shfl_sync(0xffffffffu, myrow, kk);
+                    const int key = pw * 32 + kk;
+                    cp_async_16(st + j * C::KV_SLOT + key * 128 + (((c ^ key) & 7) << 4),
+                                kv + row * kAttnDqk + rank * 256 + lane * 8);
                 }
                 // rope: 8 keys (64 bytes each) per warp instruction
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const int kl = (t & 3) * 8 + (lane >> 2), cc = lane & 3;
-                    const long long row = __shfl_sync(0xffffffffu, myrow[t >> 2], kl);
-                    const int key = (t >> 2) * 32 + kl;
+                for (int t = 0; t < 4; ++t) {
+                    const int kl = t * 8 + (lane >> 2), cc = lane & 3;
+                    const long long row = __shfl_sync(0xffffffffu, myrow, kl);
+                    const int key = pw * 32 + kl;
                     cp_async_16(st + 4 * C::KV_SLOT + key * 64 + (((cc ^ (key >> 1)) & 3) << 4),
                                 kv + row * kAttnDqk + 512 + rank * 32 + cc * 8);
                 }
