@@ -168,7 +168,11 @@ int run_index_scores(const dsa_params* p, const void* q_idx, const float* w, con
 int run_topk(const dsa_params* p, const float* scores, long long ld, const RowSpec& rs, int rows, int* idx,
              cudaStream_t st) {
     if (rs.max_len <= kTopkSmemKeys) {
-        topk_smem_kernel<<<rows, kTopkThreads, topk_smem_bytes(rs.max_len), st>>>(rs, scores, ld, p->topk, idx);
+        DevInfo* di = nullptr;
+        const int rc = device_info(&di);
+        if (rc != DSA_OK) return rc;
+        const int grid = std::max(1, std::min(rows, di->sm_count));
+        topk_smem_kernel<<<grid, kTopkThreads, topk_smem_bytes(rs.max_len), st>>>(rs, scores, ld, p->topk, rows, idx);
     } else {
         topk_kernel<<<rows, kTopkThreads, 0, st>>>(rs, scores, ld, p->topk, idx);
     }

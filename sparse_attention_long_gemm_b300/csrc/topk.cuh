@@ -5,13 +5,16 @@
 // (all of them when there are at most index_topk).  Equal scores go to the
 // lower position.  Output: ascending positions, -1 padded.
 //
-// topk_smem_kernel (rows of at most kTopkSmemKeys positions): one CTA of 1024
-// threads per row reads the row from HBM ONCE, keeping its keys in shared
-// memory, so the two refining radix passes and the emit pass cost a few
-// shared-memory instructions per element instead of global re-reads and
-// block-wide scans per 4096 elements: the emit pass gives each warp a
-// contiguous segment of positions, counts per warp, scans the 32 warp counts
-// once, and writes each warp's selections in order with ballots.
+// topk_smem_kernel (rows of at most kTopkSmemKeys positions): persistent CTAs
+// of 1024 threads, one row at a time, each row read from HBM ONCE (prefetched
+// into L2 while the CTA works on its previous row) with its keys kept in
+// shared memory.  After the first histogram, the positions whose top key bits
+// reach the k-th largest key's bin are listed in position order; the two
+// refining radix passes and the ordered emit then run over that short list.
+// Rows with too many such positions (heavy ties) refine and emit over all
+// keys instead: the emit pass gives each warp a contiguous segment of
+// positions, counts per warp, scans the 32 warp counts once, and writes each
+// warp's selections in order with ballots.
 //
 // topk_kernel (any row length; used for rows longer than the shared-memory
 // capacity, e.g. long decode caches): one CTA (1024 threads) per row.  Scores
@@ -167,76 +170,45 @@ topk_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int k, i
 
 constexpr int kTopkSmemKeys = 50 * 1024;   // keys held in shared memory (200 KB)
 constexpr int kTopkBins = 2048;
+constexpr int kTopkCand = 4096;            // candidate positions kept for the refining passes
 
 __host__ __device__ constexpr size_t topk_smem_bytes(int max_len) {
-    return static_cast<size_t>((max_len + 3) / 4 * 4) * 4 + kTopkBins * 4 + 64 * 4 + 64;
+    return static_cast<size_t>((max_len + 3) / 4 * 4) * 4 + kTopkBins * 4 + kTopkCand * 4 + 64 * 4 + 64;
 }
 
+// Prefetches `bytes` (a multiple of 16, 16-byte aligned source) of global memory into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Persistent: CTA c takes rows c, c + gridDim.x, ...  One thread prefetches the CTA's next row
+// into L2 while the current row is processed, so the HBM read of a row overlaps the work on the
+// previous one.
+//
+// Per row:
+//   pass 1   reads the row (the only HBM read of it), keeps its order-preserving keys in shared
+//            memory and counts the top 11 key bits;
+//   then     the bin B holding the k-th largest key is found.  Every key above the row's k-th
+//            largest has top bits >= B, so when the keys with top bits >= B ("candidates") are
+//            few, one ordered pass writes their positions, in position order, to a list, and the
+//            two refining radix passes and the emit run over that list only.  Rows with more
+//            candidates than the list holds (heavy ties) take the same passes over all keys.
 __global__ void __launch_bounds__(kTopkThreads)
-topk_smem_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int k, int* __restrict__ idx_out) {
+topk_smem_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int k, int rows,
+                 int* __restrict__ idx_out) {
     extern __shared__ __align__(16) uint8_t tk_smem[];
     const int n_cap = (rs.max_len + 3) / 4 * 4;
     uint32_t* keys = reinterpret_cast<uint32_t*>(tk_smem);
     uint32_t* hist = keys + n_cap;
-    uint32_t* s_cnt = hist + kTopkBins;            // [32] gt counts, [32] eq counts per warp
-    uint32_t* s_misc = s_cnt + 64;                 // digit, above
-
-    const int r = blockIdx.x;
+    uint32_t* cand = hist + kTopkBins;             // candidate positions, ascending
+    uint32_t* s_cnt = cand + kTopkCand;            // [32] gt counts, [32] eq counts per warp
+    uint32_t* s_misc = s_cnt + 64;                 // digit, keys above it, its count
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    int* out = idx_out + static_cast<long long>(r) * k;
-    const RowInfo ri = row_info(rs, r);
-    const int n = ri.ok ? ri.n : 0;
-    if (n <= k) {  // every candidate is kept (or the row is invalid: all -1)
-        for (int i = tid; i < k; i += kTopkThreads) out[i] = (i < n) ? i : -1;
-        return;
-    }
-    const float4* row4 = reinterpret_cast<const float4*>(scores + static_cast<long long>(r) * ld);
-    const int n4 = (n + 3) >> 2;
     uint4* keys4 = reinterpret_cast<uint4*>(keys);
 
-    // pass 1: the only read of the row (HBM): keys to shared memory, histogram of the top 11 bits
-    for (int i = tid; i < kTopkBins; i += kTopkThreads) hist[i] = 0u;
-    __syncthreads();
-    for (int i4 = tid; i4 < n4; i4 += kTopkThreads) {
-        const float4 v = __ldcs(row4 + i4);        // streamed: every score is read once
-        uint4 kk = make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
-        const int base = i4 * 4;
-        if (base + 3 >= n) {   // the row's ragged tail: positions past n rank below everything
-            if (base + 1 >= n) kk.y = 0u;
-            if (base + 2 >= n) kk.z = 0u;
-            if (base + 3 >= n) kk.w = 0u;
-        }
-        keys4[i4] = kk;
-        atomicAdd(&hist[kk.x >> 21], 1u);
-        if (base + 1 < n) atomicAdd(&hist[kk.y >> 21], 1u);
-        if (base + 2 < n) atomicAdd(&hist[kk.z >> 21], 1u);
-        if (base + 3 < n) atomicAdd(&hist[kk.w >> 21], 1u);
-    }
-    __syncthreads();
-
-    uint32_t prefix = 0, need = static_cast<uint32_t>(k);
-#pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = (pass == 0) ? 21 : (pass == 1 ? 10 : 0);
-        const int bits = (pass == 2) ? 10 : 11;
-        const int nb = 1 << bits;
-        if (pass > 0) {
-            // histogram of the next digit over the keys that match the prefix found so far
-            const int hi_shift = shift + bits;
-            for (int i = tid; i < nb; i += kTopkThreads) hist[i] = 0u;
-            __syncthreads();
-            const uint32_t mask = static_cast<uint32_t>(nb - 1);
-            for (int i4 = tid; i4 < n4; i4 += kTopkThreads) {
-                const uint4 kk = keys4[i4];
-                const int base = i4 * 4;
-                if ((kk.x >> hi_shift) == prefix) atomicAdd(&hist[(kk.x >> shift) & mask], 1u);
-                if ((kk.y >> hi_shift) == prefix && base + 1 < n) atomicAdd(&hist[(kk.y >> shift) & mask], 1u);
-                if ((kk.z >> hi_shift) == prefix && base + 2 < n) atomicAdd(&hist[(kk.z >> shift) & mask], 1u);
-                if ((kk.w >> hi_shift) == prefix && base + 3 < n) atomicAdd(&hist[(kk.w >> shift) & mask], 1u);
-            }
-            __syncthreads();
-        }
-        // the bin that holds the need-th largest key (thread t owns bins from the top)
+    // Finds, from the histogram of `nb` bins, the bin holding the need-th largest key, the
+    // number of keys above it and the bin's own count (thread t owns bins from the top).
+    auto find_bin = [&](int nb, uint32_t need, uint32_t* digit, uint32_t* above_out, uint32_t* count) {
         const int per = nb / kTopkThreads;   // 2 or 1
         uint32_t cnt[2] = {0u, 0u};
         for (int e = 0; e < per; ++e) cnt[e] = hist[nb - 1 - tid * per - e];
@@ -246,49 +218,169 @@ topk_smem_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int
             if (above < need && need <= above + cnt[e]) {
                 s_misc[0] = static_cast<uint32_t>(nb - 1 - tid * per - e);
                 s_misc[1] = above;
+                s_misc[2] = cnt[e];
             }
             above += cnt[e];
         }
         __syncthreads();
-        prefix = (prefix << bits) | s_misc[0];
-        need -= s_misc[1];
+        *digit = s_misc[0];
+        *above_out = s_misc[1];
+        *count = s_misc[2];
         __syncthreads();
-    }
-    const uint32_t T = prefix;   // key of the k-th largest score; `need` keys equal to T are kept
+    };
 
-    // emit: warp w owns positions [w*seg, (w+1)*seg); count, scan the warp counts, write in order
-    const int seg = ((n4 + 31) / 32) * 4;
-    const int p0 = wid * seg, p1 = min(n, p0 + seg);
-    uint32_t c_gt = 0, c_eq = 0;
-    for (int p = p0 + lane; p < p1; p += 32) {
-        const uint32_t kk = keys[p];
-        c_gt += (kk > T) ? 1u : 0u;
-        c_eq += (kk == T) ? 1u : 0u;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        c_gt += __shfl_xor_sync(0xffffffffu, c_gt, o);
-        c_eq += __shfl_xor_sync(0xffffffffu, c_eq, o);
-    }
-    if (lane == 0) { s_cnt[wid] = c_gt; s_cnt[32 + wid] = c_eq; }
-    __syncthreads();
-    uint32_t gt_before = 0, eq_before = 0;
-    for (int w = 0; w < wid; ++w) { gt_before += s_cnt[w]; eq_before += s_cnt[32 + w]; }
-    for (int base = p0; base < p1; base += 32) {
-        const int p = base + lane;
-        const uint32_t kk = (p < p1) ? keys[p] : 0u;
-        const bool gt = (p < p1) && kk > T;
-        const bool eq = (p < p1) && kk == T;
-        const uint32_t mgt = __ballot_sync(0xffffffffu, gt), meq = __ballot_sync(0xffffffffu, eq);
-        const uint32_t lt_mask = (1u << lane) - 1u;
-        const uint32_t my_eq = eq_before + __popc(meq & lt_mask);       // equal keys before p
-        const bool take = gt || (eq && my_eq < need);
-        if (take) {
-            const uint32_t slot = gt_before + __popc(mgt & lt_mask) + min(my_eq, need);
-            out[slot] = p;
+    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+        int* out = idx_out + static_cast<long long>(r) * k;
+        const RowInfo ri = row_info(rs, r);
+        const int n = ri.ok ? ri.n : 0;
+        if (tid == 0 && r + static_cast<int>(gridDim.x) < rows) {
+            const RowInfo rn = row_info(rs, r + gridDim.x);
+            const int nn = rn.ok ? rn.n : 0;
+            if (nn > k)
+                prefetch_l2_bulk(scores + static_cast<long long>(r + gridDim.x) * ld,
+                                 static_cast<uint32_t>((nn + 3) / 4) * 16u);
         }
-        gt_before += __popc(mgt);
-        eq_before += __popc(meq);
+        if (n <= k) {  // every candidate is kept (or the row is invalid: all -1)
+            for (int i = tid; i < k; i += kTopkThreads) out[i] = (i < n) ? i : -1;
+            continue;
+        }
+        const float4* row4 = reinterpret_cast<const float4*>(scores + static_cast<long long>(r) * ld);
+        const int n4 = (n + 3) >> 2;
+
+        // pass 1: keys to shared memory, histogram of the top 11 bits
+        for (int i = tid; i < kTopkBins; i += kTopkThreads) hist[i] = 0u;
+        __syncthreads();
+        for (int i4 = tid; i4 < n4; i4 += kTopkThreads) {
+            const float4 v = __ldcs(row4 + i4);        // streamed: every score is read once from DRAM
+            uint4 kk = make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+            const int base = i4 * 4;
+            if (base + 3 >= n) {   // the row's ragged tail: positions past n rank below everything
+                if (base + 1 >= n) kk.y = 0u;
+                if (base + 2 >= n) kk.z = 0u;
+                if (base + 3 >= n) kk.w = 0u;
+            }
+            keys4[i4] = kk;
+            atomicAdd(&hist[kk.x >> 21], 1u);
+            if (base + 1 < n) atomicAdd(&hist[kk.y >> 21], 1u);
+            if (base + 2 < n) atomicAdd(&hist[kk.z >> 21], 1u);
+            if (base + 3 < n) atomicAdd(&hist[kk.w >> 21], 1u);
+        }
+        __syncthreads();
+        uint32_t prefix, above, in_bin;
+        find_bin(kTopkBins, static_cast<uint32_t>(k), &prefix, &above, &in_bin);
+        uint32_t need = static_cast<uint32_t>(k) - above;
+        const uint32_t ncand = above + in_bin;           // keys with top bits >= prefix
+        const bool listed = ncand <= static_cast<uint32_t>(kTopkCand);
+        // warp w owns positions [w*seg, (w+1)*seg)
+        const int seg = ((n4 + 31) / 32) * 4;
+        const int p0 = wid * seg, p1 = min(n, p0 + seg);
+        if (listed) {
+            // the candidates' positions, in position order
+            const uint32_t B = prefix;
+            uint32_t c = 0;
+            for (int p = p0 + lane; p < p1; p += 32) c += ((keys[p] >> 21) >= B) ? 1u : 0u;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+            if (lane == 0) s_cnt[wid] = c;
+            __syncthreads();
+            uint32_t before = 0;
+            for (int w = 0; w < wid; ++w) before += s_cnt[w];
+            for (int base = p0; base < p1; base += 32) {
+                const int p = base + lane;
+                const bool cd = (p < p1) && (keys[p] >> 21) >= B;
+                const uint32_t m = __ballot_sync(0xffffffffu, cd);
+                if (cd) cand[before + __popc(m & ((1u << lane) - 1u))] = static_cast<uint32_t>(p);
+                before += __popc(m);
+            }
+            __syncthreads();
+        }
+        // passes 2 and 3: the next 11 and 10 bits, over the keys that match the prefix found so far
+#pragma unroll 1
+        for (int pass = 1; pass < 3; ++pass) {
+            const int shift = (pass == 1) ? 10 : 0;
+            const int bits = (pass == 2) ? 10 : 11;
+            const int nb = 1 << bits;
+            const int hi_shift = shift + bits;
+            const uint32_t mask = static_cast<uint32_t>(nb - 1);
+            for (int i = tid; i < nb; i += kTopkThreads) hist[i] = 0u;
+            __syncthreads();
+            if (listed) {
+                for (int j = tid; j < static_cast<int>(ncand); j += kTopkThreads) {
+                    const uint32_t kk = keys[cand[j]];
+                    if ((kk >> hi_shift) == prefix) atomicAdd(&hist[(kk >> shift) & mask], 1u);
+                }
+            } else {
+                for (int i4 = tid; i4 < n4; i4 += kTopkThreads) {
+                    const uint4 kk = keys4[i4];
+                    const int base = i4 * 4;
+                    if ((kk.x >> hi_shift) == prefix) atomicAdd(&hist[(kk.x >> shift) & mask], 1u);
+                    if ((kk.y >> hi_shift) == prefix && base + 1 < n) atomicAdd(&hist[(kk.y >> shift) & mask], 1u);
+                    if ((kk.z >> hi_shift) == prefix && base + 2 < n) atomicAdd(&hist[(kk.z >> shift) & mask], 1u);
+                    if ((kk.w >> hi_shift) == prefix && base + 3 < n) atomicAdd(&hist[(kk.w >> shift) & mask], 1u);
+                }
+            }
+            __syncthreads();
+            uint32_t digit, ab, nbin;
+            find_bin(nb, need, &digit, &ab, &nbin);
+            (void)nbin;
+            prefix = (prefix << bits) | digit;
+            need -= ab;
+        }
+        const uint32_t T = prefix;   // key of the k-th largest score; `need` keys equal to T are kept
+
+        if (listed) {
+            // emit over the candidate list (position order): keys > T and the first `need` == T
+            uint32_t sel_seen = 0, eq_seen = 0;
+            for (int base = 0; base < static_cast<int>(ncand); base += kTopkThreads) {
+                const int j = base + tid;
+                const bool valid = j < static_cast<int>(ncand);
+                const uint32_t p = valid ? cand[j] : 0u;
+                const uint32_t kk = valid ? keys[p] : 0u;
+                const bool gt = valid && kk > T, eq = valid && kk == T;
+                uint32_t tot;
+                const uint32_t pre = block_excl_scan((gt ? 1u : 0u) | ((eq ? 1u : 0u) << 16), s_cnt, &tot);
+                const uint32_t gt_before = pre & 0xffffu, eq_before = pre >> 16;
+                const uint32_t rem = (need > eq_seen) ? need - eq_seen : 0u;   // equal keys still to keep
+                if (gt || (eq && eq_before < rem))
+                    out[sel_seen + gt_before + min(eq_before, rem)] = static_cast<int>(p);
+                sel_seen += (tot & 0xffffu) + min(tot >> 16, rem);
+                eq_seen += tot >> 16;
+            }
+        } else {
+            // emit over all keys: count per warp, scan the warp counts, write in order
+            uint32_t c_gt = 0, c_eq = 0;
+            for (int p = p0 + lane; p < p1; p += 32) {
+                const uint32_t kk = keys[p];
+                c_gt += (kk > T) ? 1u : 0u;
+                c_eq += (kk == T) ? 1u : 0u;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                c_gt += __shfl_xor_sync(0xffffffffu, c_gt, o);
+                c_eq += __shfl_xor_sync(0xffffffffu, c_eq, o);
+            }
+            if (lane == 0) { s_cnt[wid] = c_gt; s_cnt[32 + wid] = c_eq; }
+            __syncthreads();
+            uint32_t gt_before = 0, eq_before = 0;
+            for (int w = 0; w < wid; ++w) { gt_before += s_cnt[w]; eq_before += s_cnt[32 + w]; }
+            for (int base = p0; base < p1; base += 32) {
+                const int p = base + lane;
+                const uint32_t kk = (p < p1) ? keys[p] : 0u;
+                const bool gt = (p < p1) && kk > T;
+                const bool eq = (p < p1) && kk == T;
+                const uint32_t mgt = __ballot_sync(0xffffffffu, gt), meq = __ballot_sync(0xffffffffu, eq);
+                const uint32_t lt_mask = (1u << lane) - 1u;
+                const uint32_t my_eq = eq_before + __popc(meq & lt_mask);       // equal keys before p
+                const bool take = gt || (eq && my_eq < need);
+                if (take) {
+                    const uint32_t slot = gt_before + __popc(mgt & lt_mask) + min(my_eq, need);
+                    out[slot] = p;
+                }
+                gt_before += __popc(mgt);
+                eq_before += __popc(meq);
+            }
+        }
+        __syncthreads();   // shared memory is reused by the next row
     }
 }
 

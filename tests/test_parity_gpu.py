@@ -75,6 +75,28 @@ def test_topk_all_equal_row_keeps_lowest_positions():
     assert np.array_equal(idx[10], np.concatenate([np.arange(11), -np.ones(k - 11)]))
 
 
+@pytest.mark.parametrize("n_eq", [3096, 3097])
+def test_topk_candidate_list_boundary(n_eq):
+    """The k-th largest key sits in a crowded top-bits bin: 1000 keys above it and n_eq equal keys
+    in it give 4096 (listed) or 4097 (refined over all keys) candidates; the equal keys, spread
+    between lower scores, must be kept lowest position first either way."""
+    k, L = 2048, 6000
+    rng = np.random.default_rng(n_eq)
+    row = np.full(L, 0.5, dtype=np.float32)
+    pos = rng.permutation(L)
+    top, eq = np.sort(pos[:1000]), np.sort(pos[1000:1000 + n_eq])
+    row[top] = (100.0 + rng.random(1000)).astype(np.float32)
+    row[eq] = 2.0
+    sc = np.tile(row, (L, 1))
+    cu = torch.tensor([0, L], dtype=torch.int32, device=DEV)
+    p = B.make_params(64, 128, 128, 576, 512, k, 0.07, "bf16")
+    idx = dsa.topk(p, torch.from_numpy(sc).to(DEV), cu, L).cpu().numpy()
+    want = np.sort(np.concatenate([top, eq[: k - 1000]]))
+    assert np.array_equal(idx[L - 1], want)
+    for t in (2047, 2048, 4500, 5998):
+        assert np.array_equal(idx[t], O.topk_select(sc[t, : t + 1], k)), t
+
+
 # ---------------------------------------------------------------------------
 # indexer scores
 # ---------------------------------------------------------------------------
