@@ -275,22 +275,47 @@ topk_smem_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int
         const int seg = ((n4 + 31) / 32) * 4;
         const int p0 = wid * seg, p1 = min(n, p0 + seg);
         if (listed) {
-            // the candidates' positions, in position order
+            // the candidates' positions, in position order: warp w owns the 4-key groups
+            // [w*seg4, (w+1)*seg4); a lane takes one group (16 bytes) per step
             const uint32_t B = prefix;
+            const int seg4 = (n4 + 31) / 32;
+            const int u0 = wid * seg4, u1 = min(n4, u0 + seg4);
+            auto flags = [&](int u, uint32_t (&f)[4]) {
+                const uint4 kk = (u < u1) ? keys4[u] : make_uint4(0u, 0u, 0u, 0u);
+                const int p = 4 * u;
+                f[0] = (u < u1 && (kk.x >> 21) >= B) ? 1u : 0u;
+                f[1] = (u < u1 && p + 1 < n && (kk.y >> 21) >= B) ? 1u : 0u;
+                f[2] = (u < u1 && p + 2 < n && (kk.z >> 21) >= B) ? 1u : 0u;
+                f[3] = (u < u1 && p + 3 < n && (kk.w >> 21) >= B) ? 1u : 0u;
+            };
             uint32_t c = 0;
-            for (int p = p0 + lane; p < p1; p += 32) c += ((keys[p] >> 21) >= B) ? 1u : 0u;
+            for (int u = u0 + lane; u < u1; u += 32) {
+                uint32_t f[4];
+                flags(u, f);
+                c += f[0] + f[1] + f[2] + f[3];
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
             if (lane == 0) s_cnt[wid] = c;
             __syncthreads();
             uint32_t before = 0;
             for (int w = 0; w < wid; ++w) before += s_cnt[w];
-            for (int base = p0; base < p1; base += 32) {
-                const int p = base + lane;
-                const bool cd = (p < p1) && (keys[p] >> 21) >= B;
-                const uint32_t m = __ballot_sync(0xffffffffu, cd);
-                if (cd) cand[before + __popc(m & ((1u << lane) - 1u))] = static_cast<uint32_t>(p);
-                before += __popc(m);
+            for (int base = u0; base < u1; base += 32) {
+                const int u = base + lane;
+                uint32_t f[4];
+                flags(u, f);
+                const uint32_t cnt = f[0] + f[1] + f[2] + f[3];
+                uint32_t incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                uint32_t slot = before + incl - cnt;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (f[e]) cand[slot++] = static_cast<uint32_t>(4 * u + e);
+                before += __shfl_sync(0xffffffffu, incl, 31);
             }
             __syncthreads();
         }
@@ -329,22 +354,38 @@ topk_smem_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int
         const uint32_t T = prefix;   // key of the k-th largest score; `need` keys equal to T are kept
 
         if (listed) {
-            // emit over the candidate list (position order): keys > T and the first `need` == T
-            uint32_t sel_seen = 0, eq_seen = 0;
-            for (int base = 0; base < static_cast<int>(ncand); base += kTopkThreads) {
-                const int j = base + tid;
-                const bool valid = j < static_cast<int>(ncand);
-                const uint32_t p = valid ? cand[j] : 0u;
-                const uint32_t kk = valid ? keys[p] : 0u;
-                const bool gt = valid && kk > T, eq = valid && kk == T;
-                uint32_t tot;
-                const uint32_t pre = block_excl_scan((gt ? 1u : 0u) | ((eq ? 1u : 0u) << 16), s_cnt, &tot);
-                const uint32_t gt_before = pre & 0xffffu, eq_before = pre >> 16;
-                const uint32_t rem = (need > eq_seen) ? need - eq_seen : 0u;   // equal keys still to keep
-                if (gt || (eq && eq_before < rem))
-                    out[sel_seen + gt_before + min(eq_before, rem)] = static_cast<int>(p);
-                sel_seen += (tot & 0xffffu) + min(tot >> 16, rem);
-                eq_seen += tot >> 16;
+            // emit over the candidate list (position order): keys > T and the first `need` == T.
+            // Warp w owns list entries [w*segc, (w+1)*segc): count, scan the warp counts, write.
+            const int segc = (static_cast<int>(ncand) + 31) / 32;
+            const int j0 = wid * segc, j1 = min(static_cast<int>(ncand), j0 + segc);
+            uint32_t c_gt = 0, c_eq = 0;
+            for (int j = j0 + lane; j < j1; j += 32) {
+                const uint32_t kk = keys[cand[j]];
+                c_gt += (kk > T) ? 1u : 0u;
+                c_eq += (kk == T) ? 1u : 0u;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                c_gt += __shfl_xor_sync(0xffffffffu, c_gt, o);
+                c_eq += __shfl_xor_sync(0xffffffffu, c_eq, o);
+            }
+            if (lane == 0) { s_cnt[wid] = c_gt; s_cnt[32 + wid] = c_eq; }
+            __syncthreads();
+            uint32_t gt_before = 0, eq_before = 0;
+            for (int w = 0; w < wid; ++w) { gt_before += s_cnt[w]; eq_before += s_cnt[32 + w]; }
+            for (int base = j0; base < j1; base += 32) {
+                const int j = base + lane;
+                const uint32_t p = (j < j1) ? cand[j] : 0u;
+                const uint32_t kk = (j < j1) ? keys[p] : 0u;
+                const bool gt = (j < j1) && kk > T;
+                const bool eq = (j < j1) && kk == T;
+                const uint32_t mgt = __ballot_sync(0xffffffffu, gt), meq = __ballot_sync(0xffffffffu, eq);
+                const uint32_t lt_mask = (1u << lane) - 1u;
+                const uint32_t my_eq = eq_before + __popc(meq & lt_mask);       // equal keys before p
+                if (gt || (eq && my_eq < need))
+                    out[gt_before + __popc(mgt & lt_mask) + min(my_eq, need)] = static_cast<int>(p);
+                gt_before += __popc(mgt);
+                eq_before += __popc(meq);
             }
         } else {
             // emit over all keys: count per warp, scan the warp counts, write in order
