@@ -82,7 +82,8 @@ int device_info(DevInfo** out) {
         set(reinterpret_cast<const void*>(&indexer_tc_kernel<kPreNQ, kPreKS, kPreQB>), IdxTc<kPreNQ, kPreKS, kPreQB>::SMEM);
         set(reinterpret_cast<const void*>(&indexer_tc_kernel<kDecNQ, kDecKS, kDecQB>), IdxTc<kDecNQ, kDecKS, kDecQB>::SMEM);
         set(reinterpret_cast<const void*>(&attn_tc_kernel), AttnTc::SMEM);
-        set(reinterpret_cast<const void*>(&topk_smem_kernel), topk_smem_bytes(kTopkSmemKeys));
+        set(reinterpret_cast<const void*>(&topk_smem_kernel<1>), topk_smem_bytes(kTopkSmemKeys));
+        set(reinterpret_cast<const void*>(&topk_smem_kernel<2>), topk_smem_bytes(kTopkSmemKeys));
         set(reinterpret_cast<const void*>(&indexer_simt_kernel<float>), indexer_simt_smem(128, 128));
         set(reinterpret_cast<const void*>(&indexer_simt_kernel<__nv_bfloat16>), indexer_simt_smem(128, 128));
         set(reinterpret_cast<const void*>(&attn_simt_kernel<float>), attn_simt_smem(1024, 16384));
@@ -171,8 +172,22 @@ int run_topk(const dsa_params* p, const float* scores, long long ld, const RowSp
         DevInfo* di = nullptr;
         const int rc = device_info(&di);
         if (rc != DSA_OK) return rc;
-        const int grid = std::max(1, std::min(rows, di->sm_count));
-        topk_smem_kernel<<<grid, kTopkThreads, topk_smem_bytes(rs.max_len), st>>>(rs, scores, ld, p->topk, rows, idx);
+        // persistent: two CTAs per SM when two rows' keys fit in shared memory together
+        // (rows up to ~22K keys), else one
+        const size_t smem = topk_smem_bytes(rs.max_len);
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_smem_kernel<2>, kTopkThreads, smem) !=
+            cudaSuccess) {
+            per_sm = 0;
+            (void)cudaGetLastError();   // a failed query only selects the one-CTA kernel
+        }
+        if (per_sm >= 2) {
+            const int grid = std::max(1, std::min(rows, 2 * di->sm_count));
+            topk_smem_kernel<2><<<grid, kTopkThreads, smem, st>>>(rs, scores, ld, p->topk, rows, idx);
+        } else {
+            const int grid = std::max(1, std::min(rows, di->sm_count));
+            topk_smem_kernel<1><<<grid, kTopkThreads, smem, st>>>(rs, scores, ld, p->topk, rows, idx);
+        }
     } else {
         topk_kernel<<<rows, kTopkThreads, 0, st>>>(rs, scores, ld, p->topk, idx);
     }

@@ -193,7 +193,11 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes
 //            few, one ordered pass writes their positions, in position order, to a list, and the
 //            two refining radix passes and the emit run over that list only.  Rows with more
 //            candidates than the list holds (heavy ties) take the same passes over all keys.
-__global__ void __launch_bounds__(kTopkThreads)
+//
+// kMinBlocks = 2 caps registers at 32 so that two CTAs share an SM (rows short enough for two
+// CTAs' shared memory); kMinBlocks = 1 leaves the compiler 64 registers for long rows.
+template <int kMinBlocks>
+__global__ void __launch_bounds__(kTopkThreads, kMinBlocks)
 topk_smem_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int k, int rows,
                  int* __restrict__ idx_out) {
     extern __shared__ __align__(16) uint8_t tk_smem[];
