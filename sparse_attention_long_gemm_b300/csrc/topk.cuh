@@ -192,7 +192,8 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes
 //            largest has top bits >= B, so when the keys with top bits >= B ("candidates") are
 //            few, one ordered pass writes their positions, in position order, to a list, and the
 //            two refining radix passes and the emit run over that list only.  Rows with more
-//            candidates than the list holds (heavy ties) take the same passes over all keys.
+//            candidates than the list holds (heavy ties), or with at least half their keys
+//            listed (short rows), take the same passes over all keys.
 //
 // kMinBlocks = 2 caps registers at 32 so that two CTAs share an SM (rows short enough for two
 // CTAs' shared memory); kMinBlocks = 1 leaves the compiler 64 registers for long rows.
@@ -274,7 +275,8 @@ topk_smem_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int
         find_bin(kTopkBins, static_cast<uint32_t>(k), &prefix, &above, &in_bin);
         uint32_t need = static_cast<uint32_t>(k) - above;
         const uint32_t ncand = above + in_bin;           // keys with top bits >= prefix
-        const bool listed = ncand <= static_cast<uint32_t>(kTopkCand);
+        // the list pays for its extra ordered pass only when it is well shorter than the row
+        const bool listed = ncand <= static_cast<uint32_t>(kTopkCand) && 2 * ncand <= static_cast<uint32_t>(n);
         // warp w owns positions [w*seg, (w+1)*seg)
         const int seg = ((n4 + 31) / 32) * 4;
         const int p0 = wid * seg, p1 = min(n, p0 + seg);

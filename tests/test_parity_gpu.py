@@ -78,9 +78,10 @@ def test_topk_all_equal_row_keeps_lowest_positions():
 @pytest.mark.parametrize("n_eq", [3096, 3097])
 def test_topk_candidate_list_boundary(n_eq):
     """The k-th largest key sits in a crowded top-bits bin: 1000 keys above it and n_eq equal keys
-    in it give 4096 (listed) or 4097 (refined over all keys) candidates; the equal keys, spread
-    between lower scores, must be kept lowest position first either way."""
-    k, L = 2048, 6000
+    in it give 4096 (listed, for the full row of 9000) or 4097 (refined over all keys)
+    candidates; the equal keys, spread between lower scores, must be kept lowest position first
+    either way."""
+    k, L = 2048, 9000
     rng = np.random.default_rng(n_eq)
     row = np.full(L, 0.5, dtype=np.float32)
     pos = rng.permutation(L)
@@ -93,7 +94,7 @@ def test_topk_candidate_list_boundary(n_eq):
     idx = dsa.topk(p, torch.from_numpy(sc).to(DEV), cu, L).cpu().numpy()
     want = np.sort(np.concatenate([top, eq[: k - 1000]]))
     assert np.array_equal(idx[L - 1], want)
-    for t in (2047, 2048, 4500, 5998):
+    for t in (2047, 2048, 5000, 8998):
         assert np.array_equal(idx[t], O.topk_select(sc[t, : t + 1], k)), t
 
 
