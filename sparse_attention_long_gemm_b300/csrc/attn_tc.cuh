@@ -69,13 +69,12 @@
 //   one warp    TMEM allocation and tcgen05.mma issue (one thread, polling
 //               both the next Q.K^T and the next P.V so neither waits on the
 //               other): warp 6 on rank 0, warp 4 on rank 1;
-//   two warps   producers (warps 5 and 7), each
-//               gathering half of the keys of every KV item by cp.async: each
-//               warp instruction one key's 512 latent bytes (the rope parts of
-//               8 keys per instruction), completion signalled with
-//               cp.async.mbarrier.arrive.noinc so the producers never wait for
-//               data; index loads run four blocks ahead; one thread issues the
-//               TMA loads of Q items.
+//   two warps   producers (warps 5 and 7), each gathering half of the keys of
+//               every KV item by cp.async: each warp instruction one key's 512
+//               latent bytes (the rope parts of 8 keys per instruction),
+//               completion signalled with cp.async.mbarrier.arrive.noinc so the
+//               producers never wait for data; index loads run four blocks
+//               ahead; one thread issues the TMA loads of Q items.
 #pragma once
 
 #include <cuda.h>
@@ -530,7 +529,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tmem_st32(tmem_base + lane_off + C::TM_O + c0, o);
             }
         };
-        // this warp's P.V of block g-2 has finished reading P buffer g & 1
+        // the P.V of block g-2 has finished reading P tile g & 1 (and O holds it)
         auto wait_p_buffer = [&](int g) -> bool {
             if (g < 2) return true;
             return __all_sync(0xffffffffu, wait_bar(pv_done(g & 1), (((g - 2) >> 1) & 1), timeout_ns, s_abort));
