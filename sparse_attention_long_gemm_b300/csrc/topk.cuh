@@ -11,15 +11,17 @@
 // shared memory.  After the first histogram, the positions whose top key bits
 // reach the k-th largest key's bin are listed in position order; the two
 // refining radix passes and the ordered emit then run over that short list.
-// Rows with too many such positions (heavy ties) refine and emit over all
-// keys instead: the emit pass gives each warp a contiguous segment of
-// positions, counts per warp, scans the 32 warp counts once, and writes each
-// warp's selections in order with ballots.
+// Rows with too many such positions (heavy ties), or whose list would hold
+// half the row or more (short rows), refine and emit over all keys instead:
+// the emit pass gives each warp a contiguous segment of positions, counts per
+// warp, scans the 32 warp counts once, and writes each warp's selections in
+// order with ballots.  Two instantiations: two CTAs per SM (32 registers) for
+// rows whose keys fit twice in shared memory, one CTA per SM otherwise.
 //
 // topk_kernel (any row length; used for rows longer than the shared-memory
 // capacity, e.g. long decode caches): one CTA (1024 threads) per row.  Scores
-// become order-preserving 32-bit keys (score_key).  Three histogram passes over 11 + 11 + 10 key bits
-// find the exact key T of the k-th largest score and how many of the
+// become order-preserving 32-bit keys (score_key).  Three histogram passes over
+// 11 + 11 + 10 key bits find the exact key T of the k-th largest score and how many of the
 // scores equal to T must be kept ("need"); a final pass in position order
 // keeps every key > T and the first `need` keys == T, computing output
 // slots with a block-wide prefix sum, so the result is sorted by position
