@@ -23,6 +23,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -284,8 +285,9 @@ def run_ours(args, cfg):
         raise RuntimeError(f"device error during warm-up: {err}")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
-        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, f"/tmp/dsa_clocks_{rank}.csv")
+    # raw samples go to DSA_CLOCKS_DIR when set (to keep them), else to the temp directory
+    clocks_dir = os.environ.get("DSA_CLOCKS_DIR") or tempfile.gettempdir()
+    sampler = ClockSampler(local, os.path.join(clocks_dir, f"dsa_clocks_rank{rank}.csv"))
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)

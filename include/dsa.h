@@ -193,7 +193,7 @@ const char* dsa_path_name(const dsa_params* params);
 
 /* Decode forward for callers that cannot allocate device memory.
  *
- * The paper has no counterpart: this is a library convenience.  Some
+ * The pages describe no such call: this is a library convenience.  Some
  * callers have no way to obtain a workspace: plug-in code that runs inside
  * another framework without access to its allocator, or a serving loop
  * whose device memory is entirely owned by a pool it does not control and
