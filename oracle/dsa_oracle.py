@@ -42,6 +42,10 @@ import numpy as np
 __all__ = [
     "index_scores_row",
     "index_scores",
+    "e4m3_round",
+    "hadamard",
+    "fp8_quantize_rows",
+    "index_scores_fp8_row",
     "topk_select",
     "additive_mask_row",
     "masked_attention_row",
@@ -99,6 +103,79 @@ def index_scores(q_idx, w, k_idx):
     for t in range(L):
         out[t, : t + 1] = index_scores_row(q[t], _f64(w[t]), _f64(k_idx[: t + 1]))
     return out
+
+
+# --------------------------------------------------------------------------
+# Step 1, FP8 form (not yet on the GPU path)
+# --------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x):
+    """Nearest FP8 E4M3 value, ties to even, saturating at +-448.
+
+    E4M3 (the "fn" variant: 1 sign, 4 exponent bits with bias 7, 3 mantissa
+    bits, no infinities): normal values m * 2^(e-3) with m in [8, 16) and
+    e in [-6, 8] (largest finite value 1.75 * 2^8 = 448); subnormal values
+    m * 2^-9 with m in [0, 8).  So in every binade the spacing is 2^(e-3),
+    and below 2^-6 it is 2^-9.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0.0, a, 1.0)))
+    e = np.clip(e, -6.0, 8.0)               # below 2^-6: the subnormal spacing 2^-9
+    quantum = np.exp2(e - 3.0)
+    v = np.round(a / quantum) * quantum     # numpy rounds halves to even
+    return np.copysign(np.minimum(v, E4M3_MAX), x)
+
+
+def hadamard(n):
+    """n x n Hadamard matrix (n a power of two) by Sylvester's construction:
+    H_1 = [1], H_2m = [[H_m, H_m], [H_m, -H_m]].  Entries are +-1 and
+    H @ H.T = n * I, so H / sqrt(n) is orthogonal (and symmetric)."""
+    if n < 1 or n & (n - 1):
+        raise ValueError("n must be a power of two")
+    h = np.ones((1, 1))
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def fp8_quantize_rows(x):
+    """Each row of x quantised to E4M3 with its own scale amax / 448:
+    returns (q8, scale) with x ~= q8 * scale[:, None] (q8 on the E4M3 grid).
+    An all-zero row gets scale 1."""
+    x = _f64(x)
+    amax = np.abs(x).max(axis=1)
+    scale = np.where(amax > 0.0, amax / E4M3_MAX, 1.0)
+    return e4m3_round(x / scale[:, None]), scale
+
+
+def index_scores_fp8_row(q_idx_t, w_t, k_idx_prefix):
+    """Index scores of one query in the indexer's FP8 form.
+
+    DeepSeek-V3.2 page, "DeepSeek Sparse Attention (DSA)", Lightning Indexer
+    paragraph: the reference implementation runs the indexer in FP8 after a
+    Hadamard transform (rotate_activation); the transform is orthogonal, so
+    Hq . Hk = q . k, and FP8 is a precision optimisation.  The pages give no
+    quantisation details; the reading here:
+      1. rotate every indexer query head and every key by the normalised
+         Hadamard matrix H / sqrt(index_head_dim);
+      2. quantise each rotated vector (one query head, one key) to E4M3 with
+         its own scale amax / 448;
+      3. I[s] = sum_j w[j] * ReLU(s_q[j] * s_k[s] * (q8[j] . k8[s])).
+
+    Shapes and result as index_scores_row.
+    """
+    q = _f64(q_idx_t)
+    w = _f64(w_t)
+    k = _f64(k_idx_prefix)
+    d = q.shape[-1]
+    rot = hadamard(d) / np.sqrt(d)
+    q8, sq = fp8_quantize_rows(q @ rot.T)
+    k8, sk = fp8_quantize_rows(k @ rot.T)
+    dots = (q8 @ k8.T) * sq[:, None] * sk[None, :]
+    return w @ np.maximum(dots, 0.0)
 
 
 # --------------------------------------------------------------------------
