@@ -95,7 +95,8 @@ typedef struct dsa_params {
  * 1 <= n_heads <= 256, 8 <= d_v <= d_qk <= 1024 (multiples of 8),
  * 1 <= topk <= 16384, max_seqlen / max_ctx <= 1048576.
  * The tensor-core path is taken for the DeepSeek-V3.2 shape in bf16
- * (64, 128, 128, 576, 512); other shapes run the general kernels. */
+ * (64, 128, 128, 576, 512), at every batch size; other shapes run the
+ * general kernels. */
 
 /* Human-readable name of a status code (static string). */
 const char* dsa_status_string(int status);
@@ -170,6 +171,27 @@ int dsa_forward_decode(const dsa_params* params, const void* q_idx, const float*
                        void* out, float* lse, int* idx_out,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* The three steps of dsa_forward_decode as separate calls (same kernels),
+ * for callers that time or replace one step.  Decode form of the arguments:
+ * row b of q_idx / w / q / scores / idx / out / lse is sequence b, whose
+ * query sits at cache position cache_seqlens[b]-1 and sees cache positions
+ * 0 .. cache_seqlens[b]-1 (all of them candidates).
+ *   dsa_index_scores_decode:  scores [batch, ld] float32 (ld >= max_ctx, a
+ *       multiple of 4), entries past cache_seqlens[b]-1 left untouched.
+ *   dsa_topk_decode:  idx [batch, topk] int32, cache positions ascending,
+ *       -1 padded; bit-exact like dsa_topk.
+ *   dsa_sparse_mla_attn_decode:  attention of q [batch, n_heads, d_qk] over
+ *       the kv_cache rows idx selects; out [batch, n_heads, d_v], lse or NULL.
+ * Cache layouts, limits and errors as for dsa_forward_decode. */
+int dsa_index_scores_decode(const dsa_params* params, const void* q_idx, const float* w,
+                            const void* idx_cache, const int* cache_seqlens, int batch,
+                            int max_ctx, float* scores, long long ld, void* stream);
+int dsa_topk_decode(const dsa_params* params, const float* scores, long long ld,
+                    const int* cache_seqlens, int batch, int max_ctx, int* idx, void* stream);
+int dsa_sparse_mla_attn_decode(const dsa_params* params, const void* q, const void* kv_cache,
+                               const int* idx, const int* cache_seqlens, int batch, int max_ctx,
+                               void* out, float* lse, void* stream);
+
 /* Synchronises `stream`, then returns and clears the device error word:
  * DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_DATA (DSA_ERR_CUDA if the
  * synchronisation itself failed). */
@@ -209,8 +231,11 @@ const char* dsa_path_name(const dsa_params* params);
  *   when idx_out is NULL, batch * topk <= DSA_NOALLOC_MAX_INDICES ints;
  *   larger problems return DSA_ERR_UNSUPPORTED before anything is enqueued.
  *   Set-up: the first call on a device (with that device current) looks up
- *   the array's device address; make that first call before any stream
- *   capture begins.
+ *   the array's device address and keeps it for the life of the process;
+ *   make that first call before any stream capture begins.  The kept
+ *   address does not survive a reset of the device (cudaDeviceReset, or the
+ *   primary context being destroyed and created again): after one, the
+ *   library must be unloaded and loaded again before this call is used.
  *   Sharing: every call on a device uses the same array and leaves the last
  *   call's contents in it; nothing in it has to start at zero (each call
  *   writes every entry it later reads).  Calls whose GPU work overlaps in

@@ -23,11 +23,14 @@ from ._binding import (  # noqa: F401
     dsa_forward_decode,
     dsa_get_device_error,
     dsa_index_scores,
+    dsa_index_scores_decode,
     dsa_path_name,
     dsa_selftest_wait_timeout,
     dsa_set_wait_timeout_ns,
     dsa_sparse_mla_attn,
+    dsa_sparse_mla_attn_decode,
     dsa_topk,
+    dsa_topk_decode,
     dsa_workspace_size,
     make_params,
     params_from_config,
@@ -100,6 +103,17 @@ def decode(p, q_idx, w, q, idx_cache, kv_cache, cache_seqlens, want_lse=True, wa
     dsa_forward_decode(p, q_idx, w, q, idx_cache, kv_cache, cache_seqlens, B, max_ctx, out, lse, idx,
                        workspace, stream)
     return out, lse, idx
+
+
+def index_scores_decode(p, q_idx, w, idx_cache, cache_seqlens, stream=None):
+    """Decode score rows [B, round_up(max_ctx, 4)] (fp32; valid for s < cache_seqlens[b] only)."""
+    import torch
+
+    B, max_ctx = idx_cache.shape[0], idx_cache.shape[1]
+    ld = _round4(max_ctx)
+    scores = torch.full((B, ld), float("nan"), dtype=torch.float32, device=q_idx.device)
+    dsa_index_scores_decode(p, q_idx, w, idx_cache, cache_seqlens, B, max_ctx, scores, ld, stream)
+    return scores
 
 
 def default_scale(qk_nope_head_dim=128, qk_rope_head_dim=64):

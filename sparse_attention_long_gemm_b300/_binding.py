@@ -40,6 +40,9 @@ EXPORTED = [
     "dsa_selftest_wait_timeout",
     "dsa_path_name",
     "dsa_forward_decode_noalloc",
+    "dsa_index_scores_decode",
+    "dsa_topk_decode",
+    "dsa_sparse_mla_attn_decode",
 ]
 
 
@@ -96,6 +99,12 @@ def lib():
         L.dsa_forward_decode.argtypes = [P, vp, vp, vp, vp, vp, vp, i, i, vp, vp, vp, vp, sz, vp]
         L.dsa_forward_decode_noalloc.restype = i
         L.dsa_forward_decode_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, i, i, vp, vp, vp, vp]
+        L.dsa_index_scores_decode.restype = i
+        L.dsa_index_scores_decode.argtypes = [P, vp, vp, vp, vp, i, i, vp, ll, vp]
+        L.dsa_topk_decode.restype = i
+        L.dsa_topk_decode.argtypes = [P, vp, ll, vp, i, i, vp, vp]
+        L.dsa_sparse_mla_attn_decode.restype = i
+        L.dsa_sparse_mla_attn_decode.argtypes = [P, vp, vp, vp, vp, i, i, vp, vp, vp]
         L.dsa_get_device_error.restype = i
         L.dsa_get_device_error.argtypes = [vp]
         L.dsa_set_wait_timeout_ns.restype = ll
@@ -195,6 +204,24 @@ def dsa_forward_decode_noalloc(p, q_idx, w, q, idx_cache, kv_cache, cache_seqlen
                                           _ptr(kv_cache), _ptr(cache_seqlens), batch, max_ctx, _ptr(out),
                                           _ptr(lse), _ptr(idx_out), _stream(stream))
     _check(rc, "dsa_forward_decode_noalloc")
+
+
+def dsa_index_scores_decode(p, q_idx, w, idx_cache, cache_seqlens, batch, max_ctx, scores, ld, stream=None):
+    rc = lib().dsa_index_scores_decode(ctypes.byref(p), _ptr(q_idx), _ptr(w), _ptr(idx_cache), _ptr(cache_seqlens),
+                                       batch, max_ctx, _ptr(scores), ld, _stream(stream))
+    _check(rc, "dsa_index_scores_decode")
+
+
+def dsa_topk_decode(p, scores, ld, cache_seqlens, batch, max_ctx, idx, stream=None):
+    rc = lib().dsa_topk_decode(ctypes.byref(p), _ptr(scores), ld, _ptr(cache_seqlens), batch, max_ctx, _ptr(idx),
+                               _stream(stream))
+    _check(rc, "dsa_topk_decode")
+
+
+def dsa_sparse_mla_attn_decode(p, q, kv_cache, idx, cache_seqlens, batch, max_ctx, out, lse=None, stream=None):
+    rc = lib().dsa_sparse_mla_attn_decode(ctypes.byref(p), _ptr(q), _ptr(kv_cache), _ptr(idx), _ptr(cache_seqlens),
+                                          batch, max_ctx, _ptr(out), _ptr(lse), _stream(stream))
+    _check(rc, "dsa_sparse_mla_attn_decode")
 
 
 def dsa_get_device_error(stream=None) -> int:

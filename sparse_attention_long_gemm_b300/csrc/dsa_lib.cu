@@ -135,24 +135,34 @@ int run_index_scores(const dsa_params* p, const void* q_idx, const float* w, con
     int rc = device_info(&di);
     if (rc != DSA_OK) return rc;
     const unsigned long long to = static_cast<unsigned long long>(g_timeout_ns.load());
-    if (is_tc_shape(p) && rs.batch <= kIdxTcMaxBatch) {
+    if (is_tc_shape(p)) {
         CUtensorMap tq, tk;
-        if (!rs.decode) {
-            using C = IdxTc<kPreNQ, kPreKS, kPreQB>;
-            if ((rc = make_tmap_bf16(&tq, q_idx, static_cast<long long>(rows) * kIdxHeads, kIdxDim, C::BN)) != DSA_OK)
-                return rc;
-            if ((rc = make_tmap_bf16(&tk, k_idx, key_rows, kIdxDim, kIdxTileKeys)) != DSA_OK) return rc;
-            indexer_tc_kernel<kPreNQ, kPreKS, kPreQB>
-                <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, rs, w, scores, ld, kPreKC, to);
-        } else {
-            using C = IdxTc<kDecNQ, kDecKS, kDecQB>;
-            if ((rc = make_tmap_bf16(&tq, q_idx, static_cast<long long>(rows) * kIdxHeads, kIdxDim, C::BN)) != DSA_OK)
-                return rc;
-            if ((rc = make_tmap_bf16(&tk, k_idx, key_rows, kIdxDim, kIdxTileKeys)) != DSA_OK) return rc;
-            indexer_tc_kernel<kDecNQ, kDecKS, kDecQB>
-                <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, rs, w, scores, ld, kDecKC, to);
+        const bool dec = rs.decode != 0;
+        const int bn = dec ? IdxTc<kDecNQ, kDecKS, kDecQB>::BN : IdxTc<kPreNQ, kPreKS, kPreQB>::BN;
+        if ((rc = make_tmap_bf16(&tq, q_idx, static_cast<long long>(rows) * kIdxHeads, kIdxDim, bn)) != DSA_OK)
+            return rc;
+        if ((rc = make_tmap_bf16(&tk, k_idx, key_rows, kIdxDim, kIdxTileKeys)) != DSA_OK) return rc;
+        // The kernel keeps a per-sequence work prefix in shared memory for at most kIdxTcMaxBatch
+        // sequences; longer batches run as consecutive launches over chunks of sequences (prefill:
+        // cu_seqlens entries hold absolute rows, so a chunk just starts further into the array;
+        // decode: `base` gives the chunk's first sequence).
+        for (int b0 = 0; b0 < rs.batch; b0 += kIdxTcMaxBatch) {
+            RowSpec ch = rs;
+            ch.lens = rs.lens + b0;
+            ch.batch = std::min(kIdxTcMaxBatch, rs.batch - b0);
+            ch.base = dec ? rs.base + b0 : 0;
+            if (!dec) {
+                using C = IdxTc<kPreNQ, kPreKS, kPreQB>;
+                indexer_tc_kernel<kPreNQ, kPreKS, kPreQB>
+                    <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, ch, w, scores, ld, kPreKC, to);
+            } else {
+                using C = IdxTc<kDecNQ, kDecKS, kDecQB>;
+                indexer_tc_kernel<kDecNQ, kDecKS, kDecQB>
+                    <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, ch, w, scores, ld, kDecKC, to);
+            }
+            if ((rc = launch_status()) != DSA_OK) return rc;
         }
-        return launch_status();
+        return DSA_OK;
     }
     const size_t sm = indexer_simt_smem(p->n_idx_heads, p->idx_dim);
     if (p->dtype == DSA_BF16)
@@ -231,6 +241,16 @@ int check_prefill_common(const dsa_params* p, const int* cu, int batch, int tota
     if (cu == nullptr || batch < 1 || total_q < 0 || max_seqlen < 1) return DSA_ERR_ARG;
     if (max_seqlen > (1 << 20)) return DSA_ERR_UNSUPPORTED;
     if (static_cast<long long>(total_q) * p->n_heads * p->d_qk > (1LL << 40)) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+// Checks shared by every decode call (sizes and the cache lengths array).
+int check_decode_common(const dsa_params* p, const int* cache_seqlens, int batch, int max_ctx) {
+    int rc = check_params(p);
+    if (rc != DSA_OK) return rc;
+    if (cache_seqlens == nullptr || batch < 1 || max_ctx < 1) return DSA_ERR_ARG;
+    if (max_ctx > (1 << 20)) return DSA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(batch) * max_ctx > (1LL << 31) / 64) return DSA_ERR_UNSUPPORTED;
     return DSA_OK;
 }
 
@@ -341,16 +361,14 @@ int dsa_forward(const dsa_params* params, const void* q_idx, const float* w, con
 int dsa_forward_decode(const dsa_params* params, const void* q_idx, const float* w, const void* q,
                        const void* idx_cache, const void* kv_cache, const int* cache_seqlens, int batch, int max_ctx,
                        void* out, float* lse, int* idx_out, void* workspace, size_t workspace_bytes, void* stream) {
-    int rc = check_params(params);
+    int rc = check_decode_common(params, cache_seqlens, batch, max_ctx);
     if (rc != DSA_OK) return rc;
     if (q_idx == nullptr || w == nullptr || q == nullptr || idx_cache == nullptr || kv_cache == nullptr ||
-        cache_seqlens == nullptr || out == nullptr || batch < 1 || max_ctx < 1)
+        out == nullptr)
         return DSA_ERR_ARG;
     if (!aligned16(q_idx) || !aligned16(w) || !aligned16(q) || !aligned16(idx_cache) || !aligned16(kv_cache) ||
         !aligned16(out) || (lse && !aligned16(lse)) || (idx_out && !aligned16(idx_out)))
         return DSA_ERR_ARG;
-    if (max_ctx > (1 << 20)) return DSA_ERR_UNSUPPORTED;
-    if (static_cast<long long>(batch) * max_ctx > (1LL << 31) / 64) return DSA_ERR_UNSUPPORTED;
     const size_t need = dsa_decode_workspace_size(params, batch, max_ctx);
     if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return DSA_ERR_WORKSPACE;
@@ -365,6 +383,43 @@ int dsa_forward_decode(const dsa_params* params, const void* q_idx, const float*
     if ((rc = run_index_scores(params, q_idx, w, idx_cache, rs, batch, key_rows, scores, ld, st)) != DSA_OK) return rc;
     if ((rc = run_topk(params, scores, ld, rs, batch, idx, st)) != DSA_OK) return rc;
     return run_attn(params, q, kv_cache, idx, rs, batch, key_rows, out, lse, st);
+}
+
+int dsa_index_scores_decode(const dsa_params* params, const void* q_idx, const float* w, const void* idx_cache,
+                            const int* cache_seqlens, int batch, int max_ctx, float* scores, long long ld,
+                            void* stream) {
+    int rc = check_decode_common(params, cache_seqlens, batch, max_ctx);
+    if (rc != DSA_OK) return rc;
+    if (q_idx == nullptr || w == nullptr || idx_cache == nullptr || scores == nullptr) return DSA_ERR_ARG;
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(idx_cache) || !aligned16(scores)) return DSA_ERR_ARG;
+    if (ld < max_ctx || ld % 4 != 0) return DSA_ERR_SHAPE;
+    const RowSpec rs{cache_seqlens, batch, 1, max_ctx};
+    return run_index_scores(params, q_idx, w, idx_cache, rs, batch, static_cast<long long>(batch) * max_ctx, scores,
+                            ld, static_cast<cudaStream_t>(stream));
+}
+
+int dsa_topk_decode(const dsa_params* params, const float* scores, long long ld, const int* cache_seqlens, int batch,
+                    int max_ctx, int* idx, void* stream) {
+    int rc = check_decode_common(params, cache_seqlens, batch, max_ctx);
+    if (rc != DSA_OK) return rc;
+    if (scores == nullptr || idx == nullptr) return DSA_ERR_ARG;
+    if (!aligned16(scores) || !aligned16(idx)) return DSA_ERR_ARG;
+    if (ld < max_ctx || ld % 4 != 0) return DSA_ERR_SHAPE;
+    const RowSpec rs{cache_seqlens, batch, 1, max_ctx};
+    return run_topk(params, scores, ld, rs, batch, idx, static_cast<cudaStream_t>(stream));
+}
+
+int dsa_sparse_mla_attn_decode(const dsa_params* params, const void* q, const void* kv_cache, const int* idx,
+                               const int* cache_seqlens, int batch, int max_ctx, void* out, float* lse,
+                               void* stream) {
+    int rc = check_decode_common(params, cache_seqlens, batch, max_ctx);
+    if (rc != DSA_OK) return rc;
+    if (q == nullptr || kv_cache == nullptr || idx == nullptr || out == nullptr) return DSA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(idx) || !aligned16(out) || (lse && !aligned16(lse)))
+        return DSA_ERR_ARG;
+    const RowSpec rs{cache_seqlens, batch, 1, max_ctx};
+    return run_attn(params, q, kv_cache, idx, rs, batch, static_cast<long long>(batch) * max_ctx, out, lse,
+                    static_cast<cudaStream_t>(stream));
 }
 
 int dsa_get_device_error(void* stream) {
@@ -442,10 +497,10 @@ extern "C" int dsa_forward_decode_noalloc(const dsa_params* params, const void* 
                                           const void* q, const void* idx_cache, const void* kv_cache,
                                           const int* cache_seqlens, int batch, int max_ctx, void* out,
                                           float* lse, int* idx_out, void* stream) {
-    int rc = check_params(params);
+    int rc = check_decode_common(params, cache_seqlens, batch, max_ctx);
     if (rc != DSA_OK) return rc;
     if (q_idx == nullptr || w == nullptr || q == nullptr || idx_cache == nullptr || kv_cache == nullptr ||
-        cache_seqlens == nullptr || out == nullptr || batch < 1 || max_ctx < 1)
+        out == nullptr)
         return DSA_ERR_ARG;
     if (!aligned16(q_idx) || !aligned16(w) || !aligned16(q) || !aligned16(idx_cache) || !aligned16(kv_cache) ||
         !aligned16(out) || (lse && !aligned16(lse)) || (idx_out && !aligned16(idx_out)))

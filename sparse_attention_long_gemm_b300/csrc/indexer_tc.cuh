@@ -40,7 +40,7 @@ constexpr int kIdxDim = 128;
 constexpr int kIdxTileKeys = 128;
 constexpr int kIdxTcThreads = 320;
 constexpr int kIdxEpiThreads = 256;      // warps 2..9
-constexpr int kIdxTcMaxBatch = 256;
+constexpr int kIdxTcMaxBatch = 256;      // sequences per launch (the host splits longer batches)
 
 // Packed fp32 pairs (sm_100 family): d = a * b + c on both halves at once.
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
@@ -119,10 +119,10 @@ struct IdxSched {
         if (rs.decode) {
             const int n = __ldg(rs.lens + b);
             const int ntiles = (n + kIdxTileKeys - 1) / kIdxTileKeys;
-            U.q_row0 = b;
+            U.q_row0 = rs.base + b;
             U.nq = 1;
             U.t0 = n - 1;
-            U.key_base = static_cast<long long>(b) * rs.max_len;
+            U.key_base = static_cast<long long>(rs.base + b) * rs.max_len;
             U.kt0 = static_cast<int>(v) * kc;
             U.kt1 = min(U.kt0 + kc, ntiles);
             return U;

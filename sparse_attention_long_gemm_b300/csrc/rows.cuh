@@ -24,6 +24,8 @@ struct RowSpec {
     int batch;
     int decode;          // 0 = packed prefill, 1 = decode over caches
     int max_len;         // max_seqlen (prefill) or max_ctx (decode)
+    int base;            // decode: sequence index of lens[0] (the indexer runs long batches in
+                         // chunks, each with lens pointing at its first sequence); 0 otherwise
 };
 
 __device__ __forceinline__ RowInfo row_info(const RowSpec& rs, int r) {

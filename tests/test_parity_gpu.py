@@ -98,6 +98,48 @@ def test_topk_candidate_list_boundary(n_eq):
         assert np.array_equal(idx[t], O.topk_select(sc[t, : t + 1], k)), t
 
 
+def _topk_rows_decode(rows, k):
+    """Top-k of each score row through the decode-form entry point (row b holds len(rows[b]) keys)."""
+    n = [len(r) for r in rows]
+    ld = (max(n) + 3) // 4 * 4
+    sc = np.full((len(rows), ld), np.nan, dtype=np.float32)
+    for b, r in enumerate(rows):
+        sc[b, : len(r)] = r
+    p = B.make_params(64, 128, 128, 576, 512, k, 0.07, "bf16")
+    idx = torch.empty((len(rows), k), dtype=torch.int32, device=DEV)
+    lens = torch.tensor(n, dtype=torch.int32, device=DEV)
+    B.dsa_topk_decode(p, torch.from_numpy(sc).to(DEV), ld, lens, len(rows), max(n), idx)
+    torch.cuda.synchronize()
+    assert B.dsa_get_device_error() == B.DSA_OK
+    return idx.cpu().numpy()
+
+
+@pytest.mark.parametrize("k", [7, 2048])
+def test_topk_bit_exact_rows_beyond_shared_memory(k):
+    """Rows longer than the shared-memory capacity of the per-row kernel (51,200 keys), the decode
+    caches' case, with exact ties, signed zeros and an all-equal row, next to short rows of the
+    same call: bit-exact against the oracle on the same array."""
+    rng = np.random.default_rng(100 + k)
+
+    def noisy(n):
+        r = rng.standard_normal(n).astype(np.float32)
+        r[::3] = np.round(r[::3] * 2) / 2                       # exact ties
+        z = rng.random(n) < 0.05
+        r[z] = np.where(rng.random(z.sum()) < 0.5, 0.0, -0.0)   # -0.0 against +0.0
+        return r
+
+    crowded = np.full(65536, 0.25, dtype=np.float32)            # the k-th key in a tie of 6000
+    hot = rng.choice(65536, size=k // 2, replace=False)
+    crowded[hot] = 3.0
+    crowded[rng.choice(65536, size=6000, replace=False)] = 1.0
+    crowded[hot] = 3.0
+    rows = [noisy(51201), noisy(65536), noisy(70000), np.full(65536, -1.25, dtype=np.float32), crowded,
+            noisy(5), noisy(k), noisy(k + 1), noisy(3000)]
+    idx = _topk_rows_decode(rows, k)
+    for b, r in enumerate(rows):
+        assert np.array_equal(idx[b], O.topk_select(r, k)), (b, len(r))
+
+
 # ---------------------------------------------------------------------------
 # indexer scores
 # ---------------------------------------------------------------------------
@@ -121,6 +163,49 @@ def _check_index_scores(cfg, rel):
 def test_index_scores_tensor_core_path():
     p = _check_index_scores(V32_SMALL, SCORE_REL)
     assert B.dsa_path_name(p) == "tcgen05"
+
+
+def test_index_scores_decode_tensor_core_path():
+    """The decode form of the tensor-core indexer (one query of 64 heads per sequence against its
+    cache), element by element; entries past the cache length stay untouched."""
+    cfg = scaled(CONFIGS["decode"], batch=5, ctx_range=(1, 3000), max_ctx=3000, topk=2048)
+    inp = make_decode_inputs(cfg, "cpu", seed=8)
+    lens = inp["lengths"]
+    lens[1] = 1
+    lens[2] = 128
+    lens[3] = 129
+    inp["cache_seqlens"] = torch.tensor(lens, dtype=torch.int32)
+    g = _to(inp)
+    p = B.params_from_config(cfg)
+    assert B.dsa_path_name(p) == "tcgen05"
+    scores = dsa.index_scores_decode(p, g["q_idx"], g["w"], g["idx_cache"], g["cache_seqlens"]).cpu().numpy()
+    for b in range(cfg.batch):
+        n = lens[b]
+        kc = inp["idx_cache"][b, :n]
+        ref = O.index_scores_row(inp["q_idx"][b], inp["w"][b], kc)
+        check_scores(scores[b, :n], ref, score_denominator(inp["q_idx"][b], inp["w"][b], kc), SCORE_REL)
+        assert np.all(np.isnan(scores[b, n:])), "entries past the cache length must stay untouched"
+
+
+def test_tensor_core_path_beyond_256_sequences():
+    """Batches longer than one indexer launch's sequence table (256) stay on the tensor cores:
+    300 packed sequences (prefill) and 300 caches (decode), scores element by element."""
+    rng = np.random.default_rng(9)
+    lens = tuple(int(x) for x in rng.integers(1, 24, size=300))
+    cfg = scaled(CONFIGS["v32"], seqlens=lens, topk=16)
+    p = _check_index_scores(cfg, SCORE_REL)
+    assert B.dsa_path_name(p) == "tcgen05"
+    dcfg = scaled(CONFIGS["decode"], batch=300, ctx_range=(1, 300), max_ctx=300, topk=16)
+    inp = make_decode_inputs(dcfg, "cpu", seed=10)
+    g = _to(inp)
+    scores = dsa.index_scores_decode(p, g["q_idx"], g["w"], g["idx_cache"], g["cache_seqlens"]).cpu().numpy()
+    for b in range(dcfg.batch):
+        n = inp["lengths"][b]
+        kc = inp["idx_cache"][b, :n]
+        ref = O.index_scores_row(inp["q_idx"][b], inp["w"][b], kc)
+        check_scores(scores[b, :n], ref, score_denominator(inp["q_idx"][b], inp["w"][b], kc), SCORE_REL)
+    # the fused forward over the same long batch, on a sample of rows
+    _check_forward(cfg, 2e-2, 2e-3, rows=list(range(0, sum(lens), 53)) + [sum(lens) - 1])
 
 
 def test_index_scores_general_path_fp32():
