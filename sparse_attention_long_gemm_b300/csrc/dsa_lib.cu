@@ -82,8 +82,7 @@ int device_info(DevInfo** out) {
         set(reinterpret_cast<const void*>(&indexer_tc_kernel<kPreNQ, kPreKS, kPreQB>), IdxTc<kPreNQ, kPreKS, kPreQB>::SMEM);
         set(reinterpret_cast<const void*>(&indexer_tc_kernel<kDecNQ, kDecKS, kDecQB>), IdxTc<kDecNQ, kDecKS, kDecQB>::SMEM);
         set(reinterpret_cast<const void*>(&attn_tc_kernel), AttnTc::SMEM);
-        set(reinterpret_cast<const void*>(&topk_smem_kernel<1>), topk_smem_bytes(kTopkSmemKeys));
-        set(reinterpret_cast<const void*>(&topk_smem_kernel<2>), topk_smem_bytes(kTopkSmemKeys));
+        set(reinterpret_cast<const void*>(&topk_rows_kernel), TkSmem::bytes(kTkMaxLen));
         set(reinterpret_cast<const void*>(&indexer_simt_kernel<float>), indexer_simt_smem(128, 128));
         set(reinterpret_cast<const void*>(&indexer_simt_kernel<__nv_bfloat16>), indexer_simt_smem(128, 128));
         set(reinterpret_cast<const void*>(&attn_simt_kernel<float>), attn_simt_smem(1024, 16384));
@@ -178,26 +177,21 @@ int run_index_scores(const dsa_params* p, const void* q_idx, const float* w, con
 
 int run_topk(const dsa_params* p, const float* scores, long long ld, const RowSpec& rs, int rows, int* idx,
              cudaStream_t st) {
-    if (rs.max_len <= kTopkSmemKeys) {
+    if (rs.max_len <= kTkMaxLen) {
         DevInfo* di = nullptr;
         const int rc = device_info(&di);
         if (rc != DSA_OK) return rc;
-        // persistent: two CTAs per SM when two rows' keys fit in shared memory together
-        // (rows up to ~22K keys), else one
-        const size_t smem = topk_smem_bytes(rs.max_len);
+        // persistent: as many 256-thread CTAs as fit on every SM (4 or 5: the bitmaps follow the
+        // longest row)
+        const int smem = TkSmem::bytes(rs.max_len);
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_smem_kernel<2>, kTopkThreads, smem) !=
-            cudaSuccess) {
-            per_sm = 0;
-            (void)cudaGetLastError();   // a failed query only selects the one-CTA kernel
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_rows_kernel, kTkThreads, smem) != cudaSuccess ||
+            per_sm < 1) {
+            per_sm = 1;
+            (void)cudaGetLastError();   // a failed query only shrinks the grid
         }
-        if (per_sm >= 2) {
-            const int grid = std::max(1, std::min(rows, 2 * di->sm_count));
-            topk_smem_kernel<2><<<grid, kTopkThreads, smem, st>>>(rs, scores, ld, p->topk, rows, idx);
-        } else {
-            const int grid = std::max(1, std::min(rows, di->sm_count));
-            topk_smem_kernel<1><<<grid, kTopkThreads, smem, st>>>(rs, scores, ld, p->topk, rows, idx);
-        }
+        const int grid = std::max(1, std::min(rows, per_sm * di->sm_count));
+        topk_rows_kernel<<<grid, kTkThreads, smem, st>>>(rs, scores, ld, p->topk, rows, idx);
     } else {
         topk_kernel<<<rows, kTopkThreads, 0, st>>>(rs, scores, ld, p->topk, idx);
     }
