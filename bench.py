@@ -523,7 +523,7 @@ def run_ours(args, cfg):
         build_library()
     if ws > 1:
         dist.barrier()
-    p = dsa.params_from_config(cfg)
+    p = dsa.params_from_config(cfg, indexer_fp8=(args.indexer == "fp8"))
     inp = make_prefill_inputs(cfg, dev, seed=rank)   # weak scaling: one independent problem per rank
     lens = inp["lengths"]
     T = sum(lens)
@@ -538,11 +538,26 @@ def run_ours(args, cfg):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (126 MB)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
+    fp8 = args.indexer == "fp8"
+    if fp8:   # the indexer's FP8 operands: rotated E4M3 codes, w * s_q, s_k
+        q8 = torch.empty((T, cfg.n_idx_heads, cfg.idx_dim), dtype=torch.uint8, device=dev)
+        wq = torch.empty((T, cfg.n_idx_heads), dtype=torch.float32, device=dev)
+        k8 = torch.empty((T, cfg.idx_dim), dtype=torch.uint8, device=dev)
+        ks = torch.empty(T, dtype=torch.float32, device=dev)
+        qev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
 
-    def step(evs=None):
+    def step(evs=None, si=None):
         if evs:
             evs[0].record(stream)
-        dsa.dsa_index_scores(p, inp["q_idx"], inp["w"], inp["k_idx"], inp["cu_seqlens"], B, T, maxL, scores, ld, sp)
+        if fp8:
+            dsa.dsa_indexer_quantize_fp8(p, inp["q_idx"], T * cfg.n_idx_heads, inp["w"], q8, wq, sp)
+            dsa.dsa_indexer_quantize_fp8(p, inp["k_idx"], T, None, k8, ks, sp)
+            if evs:
+                qev[si].record(stream)
+            dsa.dsa_index_scores_fp8(p, q8, wq, k8, ks, inp["cu_seqlens"], B, T, maxL, scores, ld, sp)
+        else:
+            dsa.dsa_index_scores(p, inp["q_idx"], inp["w"], inp["k_idx"], inp["cu_seqlens"], B, T, maxL, scores, ld,
+                                 sp)
         if evs:
             evs[1].record(stream)
         dsa.dsa_topk(p, scores, ld, inp["cu_seqlens"], B, T, maxL, idx, sp)
@@ -569,11 +584,12 @@ def run_ours(args, cfg):
     torch.cuda.synchronize(dev)
     for s in range(args.steps):
         flush.zero_()          # L2 flushed between steps (not inside the timed events)
-        step(evs[s])
+        step(evs[s], s)
     torch.cuda.synchronize(dev)
     if ws > 1:
         dist.barrier()
     st = [[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs]
+    quant_ms = statistics.median(evs[i][0].elapsed_time(qev[i]) for i in range(args.steps)) if fp8 else 0.0
     extra = clock_tail(step, flush, dev, [sum(x) for x in st])
     clocks = sampler.stop()
     if clocks is not None:
@@ -636,6 +652,11 @@ def run_ours(args, cfg):
     peak_t = peaks["bf16_tflops"]
     peak_s = peaks["bf16_tflops_sustained"]
     traffic = _attn_traffic(cfg)
+    if fp8:
+        # the FP8 scores contraction alone, against the FP8 peak (the measured bf16 peak times the
+        # nominal fp8 / bf16 ratio of 2)
+        idx_tf = causal * flop_per_pair_idx(cfg) / ((stage_ms[0] - quant_ms) * 1e-3) / 1e12
+        qbytes = T * (cfg.n_idx_heads + 1) * cfg.idx_dim * 3 + T * (cfg.n_idx_heads * 8 + 4)
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, args)
@@ -654,10 +675,16 @@ def run_ours(args, cfg):
         "data": "synthetic",
         "config": {"workload": _workload_desc(cfg, lens), "l2": "flushed (256 MB write) between timed steps",
                    "per_rank": "independent problem per rank (seed = rank)",
-                   "timing": f"median of {args.steps} steps, CUDA events per stage"},
+                   "timing": f"median of {args.steps} steps, CUDA events per stage",
+                   "indexer": "FP8 (Hadamard rotation, E4M3)" if fp8 else cfg.dtype},
         "stages": {
-            "index_scores": {"ms": stage_ms[0], "tflops": idx_tf, "frac_of_peak": idx_tf / peak_t,
-                             "frac_of_sustained": idx_tf / peak_s},
+            "index_scores": ({"ms": stage_ms[0], "quantize_ms": quant_ms,
+                              "quantize_gbs": qbytes / (quant_ms * 1e-3) / 1e9 if fp8 else None,
+                              "scores_ms": stage_ms[0] - quant_ms, "tflops": idx_tf,
+                              "frac_of_peak": idx_tf / (2 * peak_t), "peak": "fp8 = 2 x measured bf16"}
+                             if fp8 else
+                             {"ms": stage_ms[0], "tflops": idx_tf, "frac_of_peak": idx_tf / peak_t,
+                              "frac_of_sustained": idx_tf / peak_s}),
             "topk": {"ms": stage_ms[1], "gbs": topk_gbs, "frac_of_peak": topk_gbs / peaks["hbm_gbs"]},
             "sparse_mla_attn": {"ms": stage_ms[2], "tflops": attn_tf, "frac_of_peak": attn_tf / peak_t,
                                 "frac_of_sustained": attn_tf / peak_s},
@@ -669,7 +696,7 @@ def run_ours(args, cfg):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clocks,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (5 if fp8 else 3) * args.steps,
         "path": dsa.dsa_path_name(p),
     }
     print(json.dumps(line), flush=True)
@@ -704,6 +731,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="long")
     ap.add_argument("--seqlen", type=int, default=0, help="override: one prefill sequence of this length")
+    ap.add_argument("--indexer", default="native", choices=["native", "fp8"],
+                    help="fp8: the indexer's FP8 form (rotation + E4M3 codes) in place of bf16")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=24)

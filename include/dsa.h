@@ -89,6 +89,8 @@ typedef struct dsa_params {
     int   topk;           /* k: tokens kept per query (index_topk)           */
     float softmax_scale;  /* multiplies q.kv before the softmax              */
     int   dtype;          /* DSA_BF16 or DSA_FP32                            */
+    int   indexer_fp8;    /* 0: step 1 in dtype; 1: step 1 in its FP8 form   */
+                          /* (dsa_forward only; see dsa_indexer_quantize_fp8) */
 } dsa_params;
 
 /* Limits: 1 <= n_idx_heads <= 128, 8 <= idx_dim <= 256 (multiple of 8),
@@ -191,6 +193,37 @@ int dsa_topk_decode(const dsa_params* params, const float* scores, long long ld,
 int dsa_sparse_mla_attn_decode(const dsa_params* params, const void* q, const void* kv_cache,
                                const int* idx, const int* cache_seqlens, int batch, int max_ctx,
                                void* out, float* lse, void* stream);
+
+/* Step 1 in its FP8 form (DeepSeek-V3.2 page, DSA section, Lightning
+ * Indexer paragraph: the reference indexer runs in FP8 after a Hadamard
+ * transform, which is orthogonal, Hq . Hk = q . k).  Reading used: every
+ * 128-d indexer query head and key is rotated by H / sqrt(128) (Sylvester
+ * order) and quantised to E4M3 (largest value 448, round to nearest even,
+ * saturating) with its own scale s = amax / 448 (1 for an all-zero vector);
+ *     I[t,s] = sum_j w[t,j] * ReLU(s_q[t,j] * s_k[s] * (q8[t,j,:] . k8[s,:])).
+ * Supported for dtype DSA_BF16, idx_dim 128 and n_idx_heads 64.
+ *
+ * dsa_indexer_quantize_fp8: rotates and quantises n_vec vectors
+ *   x [n_vec, 128] bf16 -> codes [n_vec, 128] (one E4M3 byte each);
+ *   out [n_vec] float32 receives s, or w[i] * s when w [n_vec] is given
+ *   (query heads: pass q_idx as [T*64, 128] and w as [T*64]).
+ * dsa_index_scores_fp8: scores from codes, laid out as dsa_index_scores
+ *   writes them: q8 [total_q, 64, 128] and wq = w * s_q [total_q, 64] from
+ *   the queries, k8 [total_q, 128] and ksc = s_k [total_q] from the keys.
+ * dsa_index_scores_fp8_decode: the decode form over an FP8 key cache
+ *   k8_cache [batch, max_ctx, 128] with scales ksc_cache [batch, max_ctx].
+ * With params->indexer_fp8 = 1, dsa_forward runs these (its workspace then
+ * also holds q8, wq, k8 and ksc: dsa_workspace_size includes them); the
+ * decode calls return DSA_ERR_UNSUPPORTED for that flag. */
+int dsa_indexer_quantize_fp8(const dsa_params* params, const void* x, long long n_vec,
+                             const float* w, void* codes, float* out, void* stream);
+int dsa_index_scores_fp8(const dsa_params* params, const void* q8, const float* wq,
+                         const void* k8, const float* ksc, const int* cu_seqlens, int batch,
+                         int total_q, int max_seqlen, float* scores, long long ld, void* stream);
+int dsa_index_scores_fp8_decode(const dsa_params* params, const void* q8, const float* wq,
+                                const void* k8_cache, const float* ksc_cache,
+                                const int* cache_seqlens, int batch, int max_ctx,
+                                float* scores, long long ld, void* stream);
 
 /* Synchronises `stream`, then returns and clears the device error word:
  * DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_DATA (DSA_ERR_CUDA if the

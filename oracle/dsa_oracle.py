@@ -46,6 +46,8 @@ __all__ = [
     "hadamard",
     "fp8_quantize_rows",
     "index_scores_fp8_row",
+    "fp8_rotate_quantize",
+    "index_scores_fp8_codes",
     "topk_select",
     "additive_mask_row",
     "masked_attention_row",
@@ -167,13 +169,25 @@ def index_scores_fp8_row(q_idx_t, w_t, k_idx_prefix):
 
     Shapes and result as index_scores_row.
     """
-    q = _f64(q_idx_t)
-    w = _f64(w_t)
-    k = _f64(k_idx_prefix)
-    d = q.shape[-1]
+    q8, sq = fp8_rotate_quantize(q_idx_t)
+    k8, sk = fp8_rotate_quantize(k_idx_prefix)
+    return index_scores_fp8_codes(q8, sq, w_t, k8, sk)
+
+
+def fp8_rotate_quantize(x):
+    """Steps 1 and 2 of the FP8 form for a set of vectors (rows of x): the
+    rotation by H / sqrt(d), then E4M3 codes with one scale amax / 448 per
+    rotated row.  Returns (codes as E4M3 values, scales)."""
+    x = _f64(x)
+    d = x.shape[-1]
     rot = hadamard(d) / np.sqrt(d)
-    q8, sq = fp8_quantize_rows(q @ rot.T)
-    k8, sk = fp8_quantize_rows(k @ rot.T)
+    return fp8_quantize_rows(x @ rot.T)
+
+
+def index_scores_fp8_codes(q8, sq, w_t, k8, sk):
+    """Step 3 of the FP8 form, from given codes and scales:
+    I[s] = sum_j w[j] * ReLU(s_q[j] * s_k[s] * (q8[j] . k8[s]))."""
+    q8, sq, w, k8, sk = (_f64(a) for a in (q8, sq, w_t, k8, sk))
     dots = (q8 @ k8.T) * sq[:, None] * sk[None, :]
     return w @ np.maximum(dots, 0.0)
 

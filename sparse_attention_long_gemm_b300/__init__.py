@@ -24,6 +24,9 @@ from ._binding import (  # noqa: F401
     dsa_get_device_error,
     dsa_index_scores,
     dsa_index_scores_decode,
+    dsa_index_scores_fp8,
+    dsa_index_scores_fp8_decode,
+    dsa_indexer_quantize_fp8,
     dsa_path_name,
     dsa_selftest_wait_timeout,
     dsa_set_wait_timeout_ns,

@@ -43,6 +43,9 @@ EXPORTED = [
     "dsa_index_scores_decode",
     "dsa_topk_decode",
     "dsa_sparse_mla_attn_decode",
+    "dsa_indexer_quantize_fp8",
+    "dsa_index_scores_fp8",
+    "dsa_index_scores_fp8_decode",
 ]
 
 
@@ -56,6 +59,7 @@ class DsaParams(ctypes.Structure):
         ("topk", ctypes.c_int),
         ("softmax_scale", ctypes.c_float),
         ("dtype", ctypes.c_int),
+        ("indexer_fp8", ctypes.c_int),
     ]
 
 
@@ -105,6 +109,12 @@ def lib():
         L.dsa_topk_decode.argtypes = [P, vp, ll, vp, i, i, vp, vp]
         L.dsa_sparse_mla_attn_decode.restype = i
         L.dsa_sparse_mla_attn_decode.argtypes = [P, vp, vp, vp, vp, i, i, vp, vp, vp]
+        L.dsa_indexer_quantize_fp8.restype = i
+        L.dsa_indexer_quantize_fp8.argtypes = [P, vp, ll, vp, vp, vp, vp]
+        L.dsa_index_scores_fp8.restype = i
+        L.dsa_index_scores_fp8.argtypes = [P, vp, vp, vp, vp, vp, i, i, i, vp, ll, vp]
+        L.dsa_index_scores_fp8_decode.restype = i
+        L.dsa_index_scores_fp8_decode.argtypes = [P, vp, vp, vp, vp, vp, i, i, vp, ll, vp]
         L.dsa_get_device_error.restype = i
         L.dsa_get_device_error.argtypes = [vp]
         L.dsa_set_wait_timeout_ns.restype = ll
@@ -119,15 +129,15 @@ def status_string(status: int) -> str:
     return lib().dsa_status_string(int(status)).decode()
 
 
-def make_params(n_idx_heads, idx_dim, n_heads, d_qk, d_v, topk, softmax_scale, dtype) -> DsaParams:
+def make_params(n_idx_heads, idx_dim, n_heads, d_qk, d_v, topk, softmax_scale, dtype, indexer_fp8=False) -> DsaParams:
     if isinstance(dtype, str):
         dtype = DSA_BF16 if dtype == "bf16" else DSA_FP32
-    return DsaParams(n_idx_heads, idx_dim, n_heads, d_qk, d_v, topk, float(softmax_scale), dtype)
+    return DsaParams(n_idx_heads, idx_dim, n_heads, d_qk, d_v, topk, float(softmax_scale), dtype, int(indexer_fp8))
 
 
-def params_from_config(cfg) -> DsaParams:
+def params_from_config(cfg, indexer_fp8=False) -> DsaParams:
     return make_params(cfg.n_idx_heads, cfg.idx_dim, cfg.n_heads, cfg.d_qk, cfg.d_v, cfg.topk,
-                       cfg.softmax_scale, cfg.dtype)
+                       cfg.softmax_scale, cfg.dtype, indexer_fp8)
 
 
 def _ptr(t):
@@ -222,6 +232,25 @@ def dsa_sparse_mla_attn_decode(p, q, kv_cache, idx, cache_seqlens, batch, max_ct
     rc = lib().dsa_sparse_mla_attn_decode(ctypes.byref(p), _ptr(q), _ptr(kv_cache), _ptr(idx), _ptr(cache_seqlens),
                                           batch, max_ctx, _ptr(out), _ptr(lse), _stream(stream))
     _check(rc, "dsa_sparse_mla_attn_decode")
+
+
+def dsa_indexer_quantize_fp8(p, x, n_vec, w, codes, out, stream=None):
+    rc = lib().dsa_indexer_quantize_fp8(ctypes.byref(p), _ptr(x), n_vec, _ptr(w), _ptr(codes), _ptr(out),
+                                        _stream(stream))
+    _check(rc, "dsa_indexer_quantize_fp8")
+
+
+def dsa_index_scores_fp8(p, q8, wq, k8, ksc, cu_seqlens, batch, total_q, max_seqlen, scores, ld, stream=None):
+    rc = lib().dsa_index_scores_fp8(ctypes.byref(p), _ptr(q8), _ptr(wq), _ptr(k8), _ptr(ksc), _ptr(cu_seqlens),
+                                    batch, total_q, max_seqlen, _ptr(scores), ld, _stream(stream))
+    _check(rc, "dsa_index_scores_fp8")
+
+
+def dsa_index_scores_fp8_decode(p, q8, wq, k8_cache, ksc_cache, cache_seqlens, batch, max_ctx, scores, ld,
+                                stream=None):
+    rc = lib().dsa_index_scores_fp8_decode(ctypes.byref(p), _ptr(q8), _ptr(wq), _ptr(k8_cache), _ptr(ksc_cache),
+                                           _ptr(cache_seqlens), batch, max_ctx, _ptr(scores), ld, _stream(stream))
+    _check(rc, "dsa_index_scores_fp8_decode")
 
 
 def dsa_get_device_error(stream=None) -> int:

@@ -16,6 +16,7 @@
 
 #include "attn_simt.cuh"
 #include "attn_tc.cuh"
+#include "indexer_fp8.cuh"
 #include "indexer_simt.cuh"
 #include "indexer_tc.cuh"
 #include "topk.cuh"
@@ -30,6 +31,8 @@ std::atomic<long long> g_timeout_ns{2000000000LL};
 constexpr int kPreNQ = 4, kPreKS = 3, kPreQB = 2, kPreKC = 32;
 // decode indexer: 1 query (64 columns), 5 key stages, 2 query buffers
 constexpr int kDecNQ = 1, kDecKS = 5, kDecQB = 2, kDecKC = 8;
+// FP8 forms: tiles are half the bytes, so more key stages fit
+constexpr int kF8PreKS = 6, kF8DecKS = 8;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
@@ -50,7 +53,14 @@ int check_params(const dsa_params* p) {
     if (p->n_heads > 256 || p->d_qk > 1024 || p->d_v > p->d_qk || p->d_qk % 8 != 0 || p->d_v % 8 != 0 || p->d_v < 8)
         return DSA_ERR_UNSUPPORTED;
     if (p->topk > 16384) return DSA_ERR_UNSUPPORTED;
+    if (p->indexer_fp8 != 0 && p->indexer_fp8 != 1) return DSA_ERR_ARG;
+    if (p->indexer_fp8 && !is_tc_shape(p)) return DSA_ERR_UNSUPPORTED;
     return DSA_OK;
+}
+
+// The FP8 form needs 128-d bf16 indexer vectors and 64 indexer heads.
+bool fp8_shape(const dsa_params* p) {
+    return p->dtype == DSA_BF16 && p->idx_dim == kIdxDim && p->n_idx_heads == kIdxHeads;
 }
 
 int cuda_status(cudaError_t e) {
@@ -81,6 +91,10 @@ int device_info(DevInfo** out) {
         };
         set(reinterpret_cast<const void*>(&indexer_tc_kernel<kPreNQ, kPreKS, kPreQB>), IdxTc<kPreNQ, kPreKS, kPreQB>::SMEM);
         set(reinterpret_cast<const void*>(&indexer_tc_kernel<kDecNQ, kDecKS, kDecQB>), IdxTc<kDecNQ, kDecKS, kDecQB>::SMEM);
+        set(reinterpret_cast<const void*>(&indexer_tc_kernel<kPreNQ, kF8PreKS, kPreQB, true>),
+            IdxTc<kPreNQ, kF8PreKS, kPreQB, true>::SMEM);
+        set(reinterpret_cast<const void*>(&indexer_tc_kernel<kDecNQ, kF8DecKS, kDecQB, true>),
+            IdxTc<kDecNQ, kF8DecKS, kDecQB, true>::SMEM);
         set(reinterpret_cast<const void*>(&attn_tc_kernel), AttnTc::SMEM);
         set(reinterpret_cast<const void*>(&topk_rows_kernel), TkSmem::bytes(kTkMaxLen));
         set(reinterpret_cast<const void*>(&indexer_simt_kernel<float>), indexer_simt_smem(128, 128));
@@ -125,6 +139,20 @@ int make_tmap_bf16(CUtensorMap* tm, const void* base, long long rows, long long 
     return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_CUDA;
 }
 
+// 2-D uint8 tensor [rows, cols] (E4M3 codes), box [box_rows, 128 bytes], 128-byte swizzle.
+int make_tmap_u8(CUtensorMap* tm, const void* base, long long rows, long long cols, int box_rows) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return DSA_ERR_CUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------------------
 // stage launchers (arguments already validated)
 // ---------------------------------------------------------------------------
@@ -153,11 +181,11 @@ int run_index_scores(const dsa_params* p, const void* q_idx, const float* w, con
             if (!dec) {
                 using C = IdxTc<kPreNQ, kPreKS, kPreQB>;
                 indexer_tc_kernel<kPreNQ, kPreKS, kPreQB>
-                    <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, ch, w, scores, ld, kPreKC, to);
+                    <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, ch, w, nullptr, scores, ld, kPreKC, to);
             } else {
                 using C = IdxTc<kDecNQ, kDecKS, kDecQB>;
                 indexer_tc_kernel<kDecNQ, kDecKS, kDecQB>
-                    <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, ch, w, scores, ld, kDecKC, to);
+                    <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, ch, w, nullptr, scores, ld, kDecKC, to);
             }
             if ((rc = launch_status()) != DSA_OK) return rc;
         }
@@ -172,6 +200,49 @@ int run_index_scores(const dsa_params* p, const void* q_idx, const float* w, con
         indexer_simt_kernel<float><<<rows, kIdxSimtThreads, sm, st>>>(rs, static_cast<const float*>(q_idx), w,
                                                                       static_cast<const float*>(k_idx),
                                                                       p->n_idx_heads, p->idx_dim, scores, ld);
+    return launch_status();
+}
+
+// FP8 form of step 1 from codes: q8 [rows, 64, 128] and k8 [key_rows, 128] E4M3, wq = w * s_q
+// [rows, 64], ksc = s_k [key_rows].
+int run_index_scores_fp8(const uint8_t* q8, const float* wq, const uint8_t* k8, const float* ksc, const RowSpec& rs,
+                         int rows, long long key_rows, float* scores, long long ld, cudaStream_t st) {
+    DevInfo* di = nullptr;
+    int rc = device_info(&di);
+    if (rc != DSA_OK) return rc;
+    const unsigned long long to = static_cast<unsigned long long>(g_timeout_ns.load());
+    CUtensorMap tq, tk;
+    const bool dec = rs.decode != 0;
+    const int bn = dec ? IdxTc<kDecNQ, kF8DecKS, kDecQB, true>::BN : IdxTc<kPreNQ, kF8PreKS, kPreQB, true>::BN;
+    if ((rc = make_tmap_u8(&tq, q8, static_cast<long long>(rows) * kIdxHeads, kIdxDim, bn)) != DSA_OK) return rc;
+    if ((rc = make_tmap_u8(&tk, k8, key_rows, kIdxDim, kIdxTileKeys)) != DSA_OK) return rc;
+    for (int b0 = 0; b0 < rs.batch; b0 += kIdxTcMaxBatch) {   // chunks of sequences, as for bf16
+        RowSpec ch = rs;
+        ch.lens = rs.lens + b0;
+        ch.batch = std::min(kIdxTcMaxBatch, rs.batch - b0);
+        ch.base = dec ? rs.base + b0 : 0;
+        if (!dec) {
+            using C = IdxTc<kPreNQ, kF8PreKS, kPreQB, true>;
+            indexer_tc_kernel<kPreNQ, kF8PreKS, kPreQB, true>
+                <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, ch, wq, ksc, scores, ld, kPreKC, to);
+        } else {
+            using C = IdxTc<kDecNQ, kF8DecKS, kDecQB, true>;
+            indexer_tc_kernel<kDecNQ, kF8DecKS, kDecQB, true>
+                <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, ch, wq, ksc, scores, ld, kDecKC, to);
+        }
+        if ((rc = launch_status()) != DSA_OK) return rc;
+    }
+    return DSA_OK;
+}
+
+// Rotation and E4M3 quantisation of n_vec 128-d bf16 vectors.
+int run_quantize_fp8(const void* x, long long n_vec, const float* w, uint8_t* codes, float* out, cudaStream_t st) {
+    if (n_vec == 0) return DSA_OK;
+    const long long per = kFp8Threads / 32;
+    const long long blocks = (n_vec + per - 1) / per;
+    if (blocks > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+    fp8_rotate_quantize_kernel<<<static_cast<unsigned>(blocks), kFp8Threads, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(x), n_vec, w, reinterpret_cast<uint32_t*>(codes), out);
     return launch_status();
 }
 
@@ -248,6 +319,13 @@ int check_decode_common(const dsa_params* p, const int* cache_seqlens, int batch
     return DSA_OK;
 }
 
+// Workspace bytes of the FP8 indexer's operands for T tokens: q8 [T,64,128], w * s_q [T,64],
+// k8 [T,128], s_k [T], each 256-byte aligned.
+long long fp8_workspace(long long T) {
+    return round_up(T * kIdxHeads * kIdxDim, 256) + round_up(T * kIdxHeads * 4, 256) + round_up(T * kIdxDim, 256) +
+           round_up(T * 4, 256);
+}
+
 }  // namespace
 
 extern "C" {
@@ -276,7 +354,7 @@ size_t dsa_workspace_size(const dsa_params* params, int total_q, int max_seqlen,
     const long long ld = round_up(max_seqlen, 4);
     const long long sc = round_up(static_cast<long long>(total_q) * ld * 4, 256);
     const long long ix = round_up(static_cast<long long>(total_q) * params->topk * 4, 256);
-    return static_cast<size_t>(sc + ix);
+    return static_cast<size_t>(sc + ix + (params->indexer_fp8 ? fp8_workspace(total_q) : 0));
 }
 
 size_t dsa_decode_workspace_size(const dsa_params* params, int batch, int max_ctx) {
@@ -347,7 +425,21 @@ int dsa_forward(const dsa_params* params, const void* q_idx, const float* w, con
                                                 round_up(static_cast<long long>(total_q) * ld * 4, 256));
     const RowSpec rs{cu_seqlens, batch, 0, max_seqlen};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if ((rc = run_index_scores(params, q_idx, w, k_idx, rs, total_q, total_q, scores, ld, st)) != DSA_OK) return rc;
+    if (params->indexer_fp8) {
+        // rotate and quantise q_I (folding s_q into w) and k_I into the workspace, then score
+        char* f8 = static_cast<char*>(workspace) + round_up(static_cast<long long>(total_q) * ld * 4, 256) +
+                   round_up(static_cast<long long>(total_q) * params->topk * 4, 256);
+        const long long T = total_q;
+        uint8_t* q8 = reinterpret_cast<uint8_t*>(f8);
+        float* wq = reinterpret_cast<float*>(f8 + round_up(T * kIdxHeads * kIdxDim, 256));
+        uint8_t* k8 = reinterpret_cast<uint8_t*>(reinterpret_cast<char*>(wq) + round_up(T * kIdxHeads * 4, 256));
+        float* ksc = reinterpret_cast<float*>(reinterpret_cast<char*>(k8) + round_up(T * kIdxDim, 256));
+        if ((rc = run_quantize_fp8(q_idx, T * kIdxHeads, w, q8, wq, st)) != DSA_OK) return rc;
+        if ((rc = run_quantize_fp8(k_idx, T, nullptr, k8, ksc, st)) != DSA_OK) return rc;
+        if ((rc = run_index_scores_fp8(q8, wq, k8, ksc, rs, total_q, total_q, scores, ld, st)) != DSA_OK) return rc;
+    } else if ((rc = run_index_scores(params, q_idx, w, k_idx, rs, total_q, total_q, scores, ld, st)) != DSA_OK) {
+        return rc;
+    }
     if ((rc = run_topk(params, scores, ld, rs, total_q, idx, st)) != DSA_OK) return rc;
     return run_attn(params, q, kv, idx, rs, total_q, total_q, out, lse, st);
 }
@@ -357,6 +449,7 @@ int dsa_forward_decode(const dsa_params* params, const void* q_idx, const float*
                        void* out, float* lse, int* idx_out, void* workspace, size_t workspace_bytes, void* stream) {
     int rc = check_decode_common(params, cache_seqlens, batch, max_ctx);
     if (rc != DSA_OK) return rc;
+    if (params->indexer_fp8) return DSA_ERR_UNSUPPORTED;   // the FP8 key cache has its own stage call
     if (q_idx == nullptr || w == nullptr || q == nullptr || idx_cache == nullptr || kv_cache == nullptr ||
         out == nullptr)
         return DSA_ERR_ARG;
@@ -414,6 +507,49 @@ int dsa_sparse_mla_attn_decode(const dsa_params* params, const void* q, const vo
     const RowSpec rs{cache_seqlens, batch, 1, max_ctx};
     return run_attn(params, q, kv_cache, idx, rs, batch, static_cast<long long>(batch) * max_ctx, out, lse,
                     static_cast<cudaStream_t>(stream));
+}
+
+int dsa_indexer_quantize_fp8(const dsa_params* params, const void* x, long long n_vec, const float* w, void* codes,
+                             float* out, void* stream) {
+    int rc = check_params(params);
+    if (rc != DSA_OK) return rc;
+    if (!fp8_shape(params)) return DSA_ERR_UNSUPPORTED;
+    if (x == nullptr || codes == nullptr || out == nullptr || n_vec < 0) return DSA_ERR_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(out) || (w && !aligned16(w))) return DSA_ERR_ARG;
+    return run_quantize_fp8(x, n_vec, w, static_cast<uint8_t*>(codes), out, static_cast<cudaStream_t>(stream));
+}
+
+int dsa_index_scores_fp8(const dsa_params* params, const void* q8, const float* wq, const void* k8, const float* ksc,
+                         const int* cu_seqlens, int batch, int total_q, int max_seqlen, float* scores, long long ld,
+                         void* stream) {
+    int rc = check_prefill_common(params, cu_seqlens, batch, total_q, max_seqlen);
+    if (rc != DSA_OK) return rc;
+    if (!fp8_shape(params)) return DSA_ERR_UNSUPPORTED;
+    if (q8 == nullptr || wq == nullptr || k8 == nullptr || ksc == nullptr || scores == nullptr) return DSA_ERR_ARG;
+    if (!aligned16(q8) || !aligned16(wq) || !aligned16(k8) || !aligned16(ksc) || !aligned16(scores))
+        return DSA_ERR_ARG;
+    if (ld < max_seqlen || ld % 4 != 0) return DSA_ERR_SHAPE;
+    if (total_q == 0) return DSA_OK;
+    const RowSpec rs{cu_seqlens, batch, 0, max_seqlen};
+    return run_index_scores_fp8(static_cast<const uint8_t*>(q8), wq, static_cast<const uint8_t*>(k8), ksc, rs, total_q,
+                                total_q, scores, ld, static_cast<cudaStream_t>(stream));
+}
+
+int dsa_index_scores_fp8_decode(const dsa_params* params, const void* q8, const float* wq, const void* k8_cache,
+                                const float* ksc_cache, const int* cache_seqlens, int batch, int max_ctx,
+                                float* scores, long long ld, void* stream) {
+    int rc = check_decode_common(params, cache_seqlens, batch, max_ctx);
+    if (rc != DSA_OK) return rc;
+    if (!fp8_shape(params)) return DSA_ERR_UNSUPPORTED;
+    if (q8 == nullptr || wq == nullptr || k8_cache == nullptr || ksc_cache == nullptr || scores == nullptr)
+        return DSA_ERR_ARG;
+    if (!aligned16(q8) || !aligned16(wq) || !aligned16(k8_cache) || !aligned16(ksc_cache) || !aligned16(scores))
+        return DSA_ERR_ARG;
+    if (ld < max_ctx || ld % 4 != 0) return DSA_ERR_SHAPE;
+    const RowSpec rs{cache_seqlens, batch, 1, max_ctx};
+    return run_index_scores_fp8(static_cast<const uint8_t*>(q8), wq, static_cast<const uint8_t*>(k8_cache), ksc_cache,
+                                rs, batch, static_cast<long long>(batch) * max_ctx, scores, ld,
+                                static_cast<cudaStream_t>(stream));
 }
 
 int dsa_get_device_error(void* stream) {
@@ -493,6 +629,7 @@ extern "C" int dsa_forward_decode_noalloc(const dsa_params* params, const void* 
                                           float* lse, int* idx_out, void* stream) {
     int rc = check_decode_common(params, cache_seqlens, batch, max_ctx);
     if (rc != DSA_OK) return rc;
+    if (params->indexer_fp8) return DSA_ERR_UNSUPPORTED;   // the FP8 key cache has its own stage call
     if (q_idx == nullptr || w == nullptr || q == nullptr || idx_cache == nullptr || kv_cache == nullptr ||
         out == nullptr)
         return DSA_ERR_ARG;

@@ -57,12 +57,16 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
     return d;
 }
 
-template <int NQ, int KSTAGES, int QBUF>
+// F8: operands are E4M3 codes (one byte per element, so a 128-d row is one 128-byte swizzled
+// row and each MMA takes K = 32) instead of bf16 (two 128-byte halves per row, K = 16).
+template <int NQ, int KSTAGES, int QBUF, bool F8 = false>
 struct IdxTc {
+    static constexpr int ESZ = F8 ? 1 : 2;                    // bytes per element
+    static constexpr int KH = F8 ? 1 : 2;                     // 128-byte parts of a 128-d row
     static constexpr int BN = NQ * kIdxHeads;                 // MMA N
-    static constexpr int Q_BYTES = BN * kIdxDim * 2;          // one query block
-    static constexpr int Q_HALF = BN * 128;                   // 64 columns (128 B) of it
-    static constexpr int K_BYTES = kIdxTileKeys * kIdxDim * 2;
+    static constexpr int Q_BYTES = BN * kIdxDim * ESZ;        // one query block
+    static constexpr int Q_HALF = BN * 128;                   // one 128-byte part of it
+    static constexpr int K_BYTES = kIdxTileKeys * kIdxDim * ESZ;
     static constexpr int K_HALF = kIdxTileKeys * 128;
     static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
     static constexpr int OFF_K = QBUF * Q_BYTES;
@@ -71,7 +75,7 @@ struct IdxTc {
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int OFF_TABLE = OFF_MISC + 16;
     static constexpr int SMEM = OFF_TABLE + (kIdxTcMaxBatch + 1) * 4 + 1024;  // + alignment slack
-    static constexpr uint32_t IDESC = idesc_bf16(128, BN, false, false);
+    static constexpr uint32_t IDESC = F8 ? idesc_e4m3(128, BN) : idesc_bf16(128, BN, false, false);
 };
 
 struct IdxUnit {
@@ -146,12 +150,15 @@ struct IdxSched {
     }
 };
 
-template <int NQ, int KSTAGES, int QBUF>
+// F8: q / k are E4M3 codes of the rotated vectors, w holds w * s_q (the query scales folded
+// in) and ksc the key scales s_k, applied per key after the head sum (both scales are positive,
+// so they commute with the ReLU).
+template <int NQ, int KSTAGES, int QBUF, bool F8 = false>
 __global__ void __launch_bounds__(kIdxTcThreads, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, RowSpec rs,
-                  const float* __restrict__ w, float* __restrict__ scores, long long ld, int kc,
-                  unsigned long long timeout_ns) {
-    using C = IdxTc<NQ, KSTAGES, QBUF>;
+                  const float* __restrict__ w, const float* __restrict__ ksc, float* __restrict__ scores,
+                  long long ld, int kc, unsigned long long timeout_ns) {
+    using C = IdxTc<NQ, KSTAGES, QBUF, F8>;
     using Sch = IdxSched<NQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -219,7 +226,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             ok = wait_bar(q_empty(qb), ((it_q / QBUF) & 1) ^ 1, timeout_ns, s_abort);
             if (!ok) break;
             mbar_expect_tx(q_full(qb), C::Q_BYTES);
-            for (int kh = 0; kh < 2; ++kh)
+            for (int kh = 0; kh < C::KH; ++kh)
                 tma_load_2d(sQ + qb * C::Q_BYTES + kh * C::Q_HALF, &tm_q, kh * 64, U.q_row0 * kIdxHeads, q_full(qb));
             for (int kt = U.kt0; kt < U.kt1; ++kt) {
                 const int s = it_k % KSTAGES;
@@ -227,7 +234,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (!ok) break;
                 mbar_expect_tx(k_full(s), C::K_BYTES);
                 const int krow = static_cast<int>(U.key_base + static_cast<long long>(kt) * kIdxTileKeys);
-                for (int kh = 0; kh < 2; ++kh)
+                for (int kh = 0; kh < C::KH; ++kh)
                     tma_load_2d(sK + s * C::K_BYTES + kh * C::K_HALF, &tm_k, kh * 64, krow, k_full(s));
                 ++it_k;
             }
@@ -253,12 +260,13 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(ab * C::BN);
 #pragma unroll
-                for (int kh = 0; kh < 2; ++kh) {
+                for (int kh = 0; kh < C::KH; ++kh) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
+                    for (int kk = 0; kk < 4; ++kk) {   // 32 bytes of K per MMA: 16 bf16 or 32 E4M3
                         const uint64_t a = sdesc_sw128(sK + s * C::K_BYTES + kh * C::K_HALF + kk * 32, 16, 1024);
                         const uint64_t b = sdesc_sw128(sQ + qb * C::Q_BYTES + kh * C::Q_HALF + kk * 32, 16, 1024);
-                        tc_mma_bf16(d, a, b, C::IDESC, (kh | kk) ? 1u : 0u);
+                        if constexpr (F8) tc_mma_e4m3(d, a, b, C::IDESC, (kh | kk) ? 1u : 0u);
+                        else tc_mma_bf16(d, a, b, C::IDESC, (kh | kk) ? 1u : 0u);
                     }
                 }
                 tc_commit(k_empty(s));
@@ -289,6 +297,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tc_fence_after();
                 const int s = kt * kIdxTileKeys + row;
                 const int q0 = half * QPH;
+                float sk = 0.f;   // F8: this key's scale (keys past the causal range are never written)
+                if constexpr (F8) {
+                    if (s <= U.t0 + U.nq - 1) sk = __ldg(ksc + U.key_base + s);
+                }
+                (void)sk;
                 if (q0 < U.nq) {   // warp-uniform
                     uint32_t v[QPH][64];
 #pragma unroll
@@ -321,8 +334,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         float acc[4];
                         unpack_f32x2(acc2[0], acc[0], acc[1]);
                         unpack_f32x2(acc2[1], acc[2], acc[3]);
-                        if (s <= U.t0 + qi)
-                            scores[static_cast<long long>(U.q_row0 + qi) * ld + s] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                        float val = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                        if constexpr (F8) val *= sk;
+                        if (s <= U.t0 + qi) scores[static_cast<long long>(U.q_row0 + qi) * ld + s] = val;
                     }
                 }
                 tc_fence_before();

@@ -26,14 +26,14 @@ def L():
 def _declared():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_and_library_exports_everything(L):
     names = _declared()
     assert "dsa_forward" in names and "dsa_forward_decode" in names
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True, check=True).stdout
-    exported = set(re.findall(r"\bT (dsa_[a-z_]+)\b", out))
+    exported = set(re.findall(r"\bT (dsa_[a-z0-9_]+)\b", out))
     missing = [n for n in names if n not in exported]
     assert not missing, missing
     assert set(B.EXPORTED) == set(names)
@@ -111,3 +111,26 @@ def test_wait_timeout_setting_is_clamped_and_returns_previous(L):
     old = B.dsa_set_wait_timeout_ns(5000)
     assert B.dsa_set_wait_timeout_ns(1) == 5000
     assert B.dsa_set_wait_timeout_ns(old) == 1000
+
+
+def test_fp8_indexer_flag_is_checked_on_the_host(L):
+    p = B.make_params(**V32, indexer_fp8=True)
+    assert B.dsa_path_name(p) == "tcgen05"
+    f = ctypes.c_void_p(0x10000)
+    # the decode calls read a bf16 indexer key cache: the FP8 flag is refused before any launch
+    rc = L.dsa_forward_decode(ctypes.byref(p), f, f, f, f, f, f, 2, 64, f, None, None, f, 1 << 30, None)
+    assert rc == B.DSA_ERR_UNSUPPORTED
+    rc = L.dsa_forward_decode_noalloc(ctypes.byref(p), f, f, f, f, f, f, 2, 64, f, None, None, None)
+    assert rc == B.DSA_ERR_UNSUPPORTED
+    # the FP8 form needs the 64 x 128 bf16 indexer
+    assert B.dsa_path_name(B.make_params(**TINY, indexer_fp8=True)) == "invalid"
+    bad = B.make_params(**V32)
+    bad.indexer_fp8 = 2
+    assert B.dsa_path_name(bad) == "invalid"
+    # the fused prefill's workspace grows by the quantised operands
+    q = B.make_params(**V32)
+    T = 100
+    extra = B.dsa_workspace_size(p, T, T, 1) - B.dsa_workspace_size(q, T, T, 1)
+    assert extra == T * 64 * 128 + 25600 + 12800 + 512   # q8, w*s_q, k8, s_k, each 256-aligned
+    tiny = B.make_params(**TINY)
+    assert L.dsa_indexer_quantize_fp8(ctypes.byref(tiny), f, 4, None, f, f, None) == B.DSA_ERR_UNSUPPORTED

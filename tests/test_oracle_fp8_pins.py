@@ -176,3 +176,18 @@ def test_fp8_pins_catch_planted_mistakes(name, fn):
 def test_fp8_pins_catch_truncating_rounding(monkeypatch):
     monkeypatch.setattr(O, "e4m3_round", _truncating_e4m3)
     assert not (_check_exact(O.index_scores_fp8_row) and _check_bound(O.index_scores_fp8_row))
+
+
+def test_fp8_scores_from_codes_reduce_to_the_plain_definition():
+    """With unit scales, scoring from given codes is the plain indexer score of those values."""
+    rng = np.random.default_rng(7)
+    g = _grid()
+    q8 = rng.choice(g[np.abs(g) <= 8], size=(6, D))
+    k8 = rng.choice(g[np.abs(g) <= 8], size=(9, D))
+    w = rng.standard_normal(6)
+    got = O.index_scores_fp8_codes(q8, np.ones(6), w, k8, np.ones(9))
+    assert np.allclose(got, O.index_scores_row(q8, w, k8), rtol=1e-12, atol=1e-12)
+    # positive scales factor out of the ReLU
+    sq, sk = rng.uniform(0.5, 2.0, 6), rng.uniform(0.5, 2.0, 9)
+    got2 = O.index_scores_fp8_codes(q8, sq, w, k8, sk)
+    assert np.allclose(got2, sk * O.index_scores_row(q8, w * sq, k8), rtol=1e-12, atol=1e-12)
