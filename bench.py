@@ -162,7 +162,7 @@ def _attn_traffic(cfg):
     kernel source has changed since the counters were taken (or for other workloads)."""
     import hashlib
 
-    if cfg.name != "long":
+    if cfg.name != "long" or tuple(cfg.seqlens) != (32768,):
         return None
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
