@@ -181,11 +181,11 @@ int run_index_scores(const dsa_params* p, const void* q_idx, const float* w, con
             if (!dec) {
                 using C = IdxTc<kPreNQ, kPreKS, kPreQB>;
                 indexer_tc_kernel<kPreNQ, kPreKS, kPreQB>
-                    <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, ch, w, nullptr, scores, ld, kPreKC, to);
+                    <<<di->sm_count, C::THREADS, C::SMEM, st>>>(tq, tk, ch, w, nullptr, scores, ld, kPreKC, to);
             } else {
                 using C = IdxTc<kDecNQ, kDecKS, kDecQB>;
                 indexer_tc_kernel<kDecNQ, kDecKS, kDecQB>
-                    <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, ch, w, nullptr, scores, ld, kDecKC, to);
+                    <<<di->sm_count, C::THREADS, C::SMEM, st>>>(tq, tk, ch, w, nullptr, scores, ld, kDecKC, to);
             }
             if ((rc = launch_status()) != DSA_OK) return rc;
         }
@@ -224,11 +224,11 @@ int run_index_scores_fp8(const uint8_t* q8, const float* wq, const uint8_t* k8, 
         if (!dec) {
             using C = IdxTc<kPreNQ, kF8PreKS, kPreQB, true>;
             indexer_tc_kernel<kPreNQ, kF8PreKS, kPreQB, true>
-                <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, ch, wq, ksc, scores, ld, kPreKC, to);
+                <<<di->sm_count, C::THREADS, C::SMEM, st>>>(tq, tk, ch, wq, ksc, scores, ld, kPreKC, to);
         } else {
             using C = IdxTc<kDecNQ, kF8DecKS, kDecQB, true>;
             indexer_tc_kernel<kDecNQ, kF8DecKS, kDecQB, true>
-                <<<di->sm_count, kIdxTcThreads, C::SMEM, st>>>(tq, tk, ch, wq, ksc, scores, ld, kDecKC, to);
+                <<<di->sm_count, C::THREADS, C::SMEM, st>>>(tq, tk, ch, wq, ksc, scores, ld, kDecKC, to);
         }
         if ((rc = launch_status()) != DSA_OK) return rc;
     }
@@ -238,9 +238,12 @@ int run_index_scores_fp8(const uint8_t* q8, const float* wq, const uint8_t* k8, 
 // Rotation and E4M3 quantisation of n_vec 128-d bf16 vectors.
 int run_quantize_fp8(const void* x, long long n_vec, const float* w, uint8_t* codes, float* out, cudaStream_t st) {
     if (n_vec == 0) return DSA_OK;
-    const long long per = kFp8Threads / 32;
-    const long long blocks = (n_vec + per - 1) / per;
-    if (blocks > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+    DevInfo* di = nullptr;
+    const int rc = device_info(&di);
+    if (rc != DSA_OK) return rc;
+    // enough warps for every vector group, at most 8 CTAs per SM (grid-stride beyond that)
+    const long long per = (kFp8Threads / 32) * kFp8VecPerWarp;
+    const long long blocks = std::min<long long>((n_vec + per - 1) / per, 8LL * di->sm_count);
     fp8_rotate_quantize_kernel<<<static_cast<unsigned>(blocks), kFp8Threads, 0, st>>>(
         static_cast<const __nv_bfloat16*>(x), n_vec, w, reinterpret_cast<uint32_t*>(codes), out);
     return launch_status();

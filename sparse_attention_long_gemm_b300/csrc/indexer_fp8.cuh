@@ -36,16 +36,8 @@ __device__ __forceinline__ uint16_t to_e4m3x2(float lo, float hi) {
     return r;
 }
 
-// x [n_vec, 128] bf16 -> codes [n_vec, 128] E4M3 and, per vector, its scale
-// (w == nullptr) or w[i] * scale (w != nullptr: query heads, w of the same
-// [n_vec] layout).
-__global__ void __launch_bounds__(kFp8Threads)
-fp8_rotate_quantize_kernel(const __nv_bfloat16* __restrict__ x, long long n_vec, const float* __restrict__ w,
-                           uint32_t* __restrict__ codes, float* __restrict__ out) {
-    const int lane = threadIdx.x & 31;
-    const long long v = static_cast<long long>(blockIdx.x) * (kFp8Threads / 32) + (threadIdx.x >> 5);
-    if (v >= n_vec) return;   // warp-uniform
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(x + v * 128) + lane);
+// One vector in registers (lane l: elements 4l .. 4l+3) -> its codes word and scale.
+__device__ __forceinline__ void fp8_rotate_quantize_one(uint2 raw, int lane, uint32_t* code, float* scale) {
     float e[4];
     {
         const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
@@ -76,11 +68,39 @@ fp8_rotate_quantize_kernel(const __nv_bfloat16* __restrict__ x, long long n_vec,
         const uint32_t lo = to_e4m3x2(e[0] / s, e[1] / s), hi = to_e4m3x2(e[2] / s, e[3] / s);
         packed = lo | (hi << 16);
     }
-    codes[v * 32 + lane] = packed;
-    if (lane == 0) {
-        // scale of the rotation H / sqrt(128): amax(y) / (448 sqrt(128)); an all-zero vector gets 1
-        const float sc = amax > 0.0f ? s * 0.08838834764831845f : 1.0f;
-        out[v] = (w != nullptr) ? __ldg(w + v) * sc : sc;
+    *code = packed;
+    // scale of the rotation H / sqrt(128): amax(y) / (448 sqrt(128)); an all-zero vector gets 1
+    *scale = amax > 0.0f ? s * 0.08838834764831845f : 1.0f;
+}
+
+constexpr int kFp8VecPerWarp = 4;   // vectors a warp loads ahead
+
+// x [n_vec, 128] bf16 -> codes [n_vec, 128] E4M3 and, per vector, its scale
+// (w == nullptr) or w[i] * scale (w != nullptr: query heads, w of the same
+// [n_vec] layout).  Each warp takes groups of kFp8VecPerWarp consecutive
+// vectors, their loads issued together.
+__global__ void __launch_bounds__(kFp8Threads)
+fp8_rotate_quantize_kernel(const __nv_bfloat16* __restrict__ x, long long n_vec, const float* __restrict__ w,
+                           uint32_t* __restrict__ codes, float* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = static_cast<long long>(gridDim.x) * (kFp8Threads / 32);
+    for (long long v0 = (static_cast<long long>(blockIdx.x) * (kFp8Threads / 32) + (threadIdx.x >> 5)) * kFp8VecPerWarp;
+         v0 < n_vec; v0 += nwarps * kFp8VecPerWarp) {   // warp-uniform
+        uint2 raw[kFp8VecPerWarp];
+#pragma unroll
+        for (int i = 0; i < kFp8VecPerWarp; ++i)
+            raw[i] = (v0 + i < n_vec) ? __ldcs(reinterpret_cast<const uint2*>(x + (v0 + i) * 128) + lane)
+                                      : make_uint2(0u, 0u);
+#pragma unroll
+        for (int i = 0; i < kFp8VecPerWarp; ++i) {
+            const long long v = v0 + i;
+            if (v >= n_vec) break;   // warp-uniform
+            uint32_t code;
+            float sc;
+            fp8_rotate_quantize_one(raw[i], lane, &code, &sc);
+            codes[v * 32 + lane] = code;
+            if (lane == 0) out[v] = (w != nullptr) ? __ldg(w + v) * sc : sc;
+        }
     }
 }
 

@@ -11,15 +11,15 @@
 // the per-head scores never leave TMEM and no cross-lane reduction is
 // needed.  Only the causal part (s <= t) is computed and written.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over work units):
+// Warp roles (64 + 128 NQ threads, one CTA per SM, persistent over work units):
 //   warp 0      TMA producer: query block (NQ*64 rows x 128, once per unit)
 //               and key tiles (128 x 128) into 128B-swizzled shared memory;
 //   warp 1      allocates TMEM and issues tcgen05.mma (one thread);
-//   warps 2..9  epilogue: two warps per TMEM lane quadrant, each taking half
-//               of the block's queries; both queries' accumulator columns are
-//               loaded before one wait, and each 64-head sum runs as four
-//               independent partial sums, so the epilogue keeps up with the
-//               MMAs instead of serialising load latency and FMA chains.
+//   warps 2..   epilogue: per TMEM lane quadrant, two warps for the 4-query
+//               bf16 prefill block (two queries each), four for the FP8 form
+//               (one query each), one in decode; a warp's queries' accumulator
+//               columns are loaded before one wait, and each 64-head sum runs
+//               as packed pairs in independent partial sums.
 // Two TMEM accumulators alternate so the epilogue of one key tile overlaps
 // the MMAs of the next.
 //
@@ -38,8 +38,7 @@ namespace dsa {
 constexpr int kIdxHeads = 64;
 constexpr int kIdxDim = 128;
 constexpr int kIdxTileKeys = 128;
-constexpr int kIdxTcThreads = 320;
-constexpr int kIdxEpiThreads = 256;      // warps 2..9
+constexpr int kIdxRoleThreads = 64;      // warp 0 TMA producer, warp 1 MMA issuer
 constexpr int kIdxTcMaxBatch = 256;      // sequences per launch (the host splits longer batches)
 
 // Packed fp32 pairs (sm_100 family): d = a * b + c on both halves at once.
@@ -64,6 +63,14 @@ struct IdxTc {
     static constexpr int ESZ = F8 ? 1 : 2;                    // bytes per element
     static constexpr int KH = F8 ? 1 : 2;                     // 128-byte parts of a 128-d row
     static constexpr int BN = NQ * kIdxHeads;                 // MMA N
+    // epilogue warps: one per TMEM lane quadrant and query of the block for the FP8 form, whose
+    // MMAs take half the time so that the epilogue must keep pace with twice the tiles; two
+    // per quadrant (two queries each) for the bf16 prefill block, one per quadrant in decode.
+    // (Each sub-partition's 16 Ki registers hold a quarter of the warps: 10 warps allow 168
+    // registers a thread, 18 allow 96.)
+    static constexpr int EPI_WARPS = F8 ? 4 * NQ : (NQ > 1 ? 2 * NQ : 4);
+    static constexpr int QPW = NQ * 4 / EPI_WARPS;            // queries per epilogue warp
+    static constexpr int THREADS = kIdxRoleThreads + 32 * EPI_WARPS;
     static constexpr int Q_BYTES = BN * kIdxDim * ESZ;        // one query block
     static constexpr int Q_HALF = BN * 128;                   // one 128-byte part of it
     static constexpr int K_BYTES = kIdxTileKeys * kIdxDim * ESZ;
@@ -154,7 +161,7 @@ struct IdxSched {
 // in) and ksc the key scales s_k, applied per key after the head sum (both scales are positive,
 // so they commute with the ReLU).
 template <int NQ, int KSTAGES, int QBUF, bool F8 = false>
-__global__ void __launch_bounds__(kIdxTcThreads, 1)
+__global__ void __launch_bounds__(IdxTc<NQ, KSTAGES, QBUF, F8>::THREADS, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, RowSpec rs,
                   const float* __restrict__ w, const float* __restrict__ ksc, float* __restrict__ scores,
                   long long ld, int kc, unsigned long long timeout_ns) {
@@ -181,7 +188,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid == 0) {
         for (int i = 0; i < QBUF; ++i) { mbar_init(q_full(i), 1); mbar_init(q_empty(i), 1); }
         for (int i = 0; i < KSTAGES; ++i) { mbar_init(k_full(i), 1); mbar_init(k_empty(i), 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(acc_full(i), 1); mbar_init(acc_empty(i), kIdxEpiThreads); }
+        for (int i = 0; i < 2; ++i) { mbar_init(acc_full(i), 1); mbar_init(acc_empty(i), 32 * C::EPI_WARPS); }
         mbar_init(done_bar, 1);
         *s_abort = 0;
         fence_mbar_init();
@@ -283,8 +290,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     } else if (warp >= 2) {
         // ---------------- epilogue ----------------
         const int quad = warp & 3;
-        const int half = (warp - 2) >> 2;          // which half of the block's queries
-        constexpr int QPH = (NQ + 1) / 2;          // queries per half
+        const int half = (warp - 2) >> 2;          // which group of the block's queries this warp takes
+        constexpr int QPH = C::QPW;                // queries per warp
         const int row = quad * 32 + lane;          // key within the tile = TMEM lane
         int it_acc = 0;
         bool ok = true;
