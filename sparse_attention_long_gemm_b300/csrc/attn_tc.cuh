@@ -48,22 +48,19 @@
 // scores (one tile), the outgoing partial scores (staged once and sent by one
 // bulk copy) and the rescale factors / denominators (two buffers each way).
 //
-// Per CTA (384 threads; the warp of a role depends on the rank):
-//   warps 0..3  softmax group, and warps 8..11 its second half: warps q and
-//   and 8..11   q+8 share TMEM lane quadrant q (heads 32q .. 32q+31), one head
-//               per thread, each thread of a head taking half of every
-//               64-key block's keys and half of the head's 256 O columns.
-//               The warps whose lanes are this rank's heads ("own" warps)
+// Per CTA (256 threads; the warp of a role depends on the rank so that the two
+// warps running the softmax have their SM sub-partitions to themselves):
+//   warps 0..3  softmax group, one head (TMEM lane) per thread.  The two
+//               warps whose lanes are this rank's heads ("own" warps)
 //               complete their scores, run the online softmax (running max
 //               updated lazily: O is rescaled only when it grows by more than
-//               2^8; the two halves of a head combine their block maxima
-//               through shared memory) and write their part of the P tile;
-//               the others ("peer" warps) send their lanes' partial scores,
-//               take the rescale factors that come with the peer's half of P
-//               (rescaling their part of those O rows first when told to), and
-//               hand that half of the tile back to the peer once its P.V has
-//               completed.  All move their part of each Q item into tensor
-//               memory and run their part of the output epilogue;
+//               2^8) and write their half of the P tile; the two others
+//               ("peer" warps) send their lanes' partial scores, take the
+//               rescale factors that come with the peer's half of P
+//               (rescaling those O rows first when told to), and hand that
+//               half of the tile back to the peer once its P.V has completed.
+//               All four move Q items into tensor memory and run the output
+//               epilogue;
 //   one warp    copy warp (warp 4 on rank 0, warp 6 on rank 1): one thread
 //               sends this rank's half of each P tile, with its factors, to
 //               the peer by bulk copy as soon as the own warps have written
@@ -91,7 +88,7 @@ constexpr int kAttnDqk = 576;
 constexpr int kAttnDv = 512;
 constexpr int kAttnBK = 64;              // selected keys per block
 constexpr int kAttnSlots = 4;            // ring slots
-constexpr int kAttnThreads = 384;           // 4 role warps + 2 x 4 softmax warps
+constexpr int kAttnThreads = 256;
 constexpr int kAttnProducers = 64;       // threads of the two producer warps
 
 struct AttnTc {
@@ -112,12 +109,10 @@ struct AttnTc {
     static constexpr int OFF_XS = OFF_XR + XB;                      // outgoing partial scores
     static constexpr int OFF_MR = OFF_XS + XB;                      // [2] received factors / denominators
     static constexpr int OFF_MS = OFF_MR + 2 * MB;                  // [2] outgoing factors / denominators
-    static constexpr int OFF_MX = OFF_MS + 2 * MB;                  // [2 blocks][2 halves][128] running-max exchange
-    static constexpr int OFF_LX = OFF_MX + 2 * 2 * kAttnHeads * 4;  // [2 halves][128] denominator exchange
-    static constexpr int OFF_BAR = OFF_LX + 2 * kAttnHeads * 4;
+    static constexpr int OFF_BAR = OFF_MS + 2 * MB;
     // full[S], empty[S], q_tm_full, s_full[2], s_free[2], p_full[2], pv_done[2],
-    // xr_full, xr_free, pr_full[2], pr_free[2], done, p_ready[2], pcopy_done[2], pair[2]
-    static constexpr int NBAR = 2 * kAttnSlots + 1 + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 2 + 1 + 2 + 2 + 2;
+    // xr_full, xr_free, pr_full[2], pr_free[2], done, p_ready[2], pcopy_done[2]
+    static constexpr int NBAR = 2 * kAttnSlots + 1 + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 2 + 1 + 2 + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;               // + alignment slack
     static constexpr int TMEM_COLS = 512;
@@ -232,8 +227,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t done_bar = bar0 + 8u * (2 * kAttnSlots + 15);
     auto p_ready = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 16 + i); };
     auto pcopy_done = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 18 + i); };
-    // the two warps of an own TMEM lane quadrant exchange their halves' block maxima through it
-    auto pair_bar = [&](int i) { return bar0 + 8u * (2 * kAttnSlots + 20 + i); };
     const uint32_t sP = sbase + C::OFF_P;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -252,20 +245,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     if (tid == 0) {
         for (int i = 0; i < kAttnSlots; ++i) { mbar_init(full(i), kAttnProducers); mbar_init(empty(i), 1); }
-        mbar_init(q_tm_full, 256);
+        mbar_init(q_tm_full, 128);
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full(i), 1);
-            mbar_init(s_free(i), 256);
-            mbar_init(p_full(i), 256);
+            mbar_init(s_free(i), 128);
+            mbar_init(p_full(i), 128);
             mbar_init(pv_done(i), 1);
             mbar_init(pr_full(i), 1);     // a local expect_tx; the peer's bulk copies complete it
             mbar_init(pr_free(i), 1);     // one arrive from the peer once its P.V of the buffer is done
-            mbar_init(p_ready(i), 4);     // one arrive per own warp: its rows of P and factors are written
+            mbar_init(p_ready(i), 2);     // one arrive per own warp: its rows of P and factors are written
             mbar_init(pcopy_done(i), 1);  // the copy warp: this rank's half has been read by its copy
         }
         mbar_init(xr_full, 1);            // a local expect_tx; the peer's bulk copy completes it
-        mbar_init(xr_free, 4);            // one arrive per own warp of the peer
-        for (int i = 0; i < 2; ++i) mbar_init(pair_bar(i), 64);   // every lane of the quadrant's two warps
+        mbar_init(xr_free, 2);            // one arrive per own warp of the peer
         mbar_init(done_bar, 1);
         *s_abort = 0;
         fence_mbar_init();
@@ -474,42 +466,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             bulk_wait_read<0>();
         }
-    } else if (warp < 4 || warp >= 8) {
-        // ---------------- softmax group / Q items / epilogue (warps 0..3 and 8..11) ----------------
-        // Warps q and q+8 share TMEM lane quadrant q (heads 32q .. 32q+31): thread half `kh` of a
-        // head handles keys 32 kh .. 32 kh + 31 of every 64-key block and O columns
-        // 128 kh .. 128 kh + 127 of this rank's 256.
-        const int quad = warp & 3, kh = warp >> 3;
-        const int h = quad * 32 + lane;              // head = TMEM lane
-        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-        const bool own = (quad >> 1) == rank;         // this lane's head has its softmax here
-        const bool lead = kh == 0;                    // issues the one-per-head operations
+    } else if (warp < 4) {
+        // ---------------- softmax group / Q items / epilogue (warps 0..3) ----------------
+        const int h = warp * 32 + lane;              // head = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const bool own = (warp >> 1) == rank;         // this lane's head has its softmax here
         const int hl = h & 63;                        // row of the head in the 64-head exchange tiles
-        const uint32_t pbar = pair_bar(quad & 1);     // exchange barrier of the two warps of an own quadrant
-        uint32_t pair_ph = 0;                         // its phases this thread has completed
-        // both halves of the quadrant have written their values (bounded wait, like every other)
-        auto pair_sync = [&]() -> bool {
-            mbar_arrive(pbar);
-            const bool okk = __all_sync(0xffffffffu, wait_bar(pbar, pair_ph & 1, timeout_ns, s_abort));
-            ++pair_ph;
-            return okk;
-        };
-        float* s_mx = reinterpret_cast<float*>(smem + C::OFF_MX);   // [b][kh][128]
-        float* s_lx = reinterpret_cast<float*>(smem + C::OFF_LX);   // [kh][128]
         int qi = 0, gi = 0, rp = 0;
         bool ok = true;
         uint32_t bulk_pending = 0;                    // this thread has issued bulk copies
 
-        // Moves this thread's half of the Q item at ring position rp_ into tensor memory (latent)
-        // and the rope buffer.
+        // Moves the Q item at ring position rp_ into tensor memory (latent) and the rope buffer.
         auto take_q = [&](int rp_) -> bool {
             const int sa = rp_ % kAttnSlots, sb = (rp_ + 1) % kAttnSlots;
             if (!__all_sync(0xffffffffu, wait_bar(full(sa), (rp_ / kAttnSlots) & 1, timeout_ns, s_abort) &&
                                              wait_bar(full(sb), ((rp_ + 1) / kAttnSlots) & 1, timeout_ns, s_abort)))
                 return false;
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                const int j = 2 * kh + jj;
+            for (int j = 0; j < 4; ++j) {
                 uint32_t v[32];
                 const uint8_t* src = smem + C::OFF_RING + ((rp_ + (j >> 1)) % kAttnSlots) * C::SLOT +
                                      (j & 1) * C::QL_TILE + h * 128;
@@ -525,29 +499,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                      (h & 63) * 64;
                 uint4* dst = reinterpret_cast<uint4*>(smem + C::OFF_QR + h * 64);
 #pragma unroll
-                for (int c = 2 * kh; c < 2 * kh + 2; ++c) dst[c] = reinterpret_cast<const uint4*>(src)[c];
+                for (int c = 0; c < 4; ++c) dst[c] = reinterpret_cast<const uint4*>(src)[c];
             }
             fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(q_tm_full);
-            named_sync(1, 256);                       // every thread has read the item
-            if (h == 0 && lead) {
+            named_sync(1, 128);                       // every thread has read the item
+            if (h == 0) {
                 mbar_arrive(empty(sa));
                 mbar_arrive(empty(sb));
             }
             return true;
         };
         auto zero_row = [&](int rr) {   // no valid selection (invalid row): zeros, lse = -inf
-            uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<long long>(rr) * kAttnHeads + h) * kAttnDv +
-                                                  rank * 256 + kh * 128);
-            for (int q = 0; q < 16; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
-            if (lse != nullptr && own && lead) lse[static_cast<long long>(rr) * kAttnHeads + h] = -INFINITY;
+            uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<long long>(rr) * kAttnHeads + h) * kAttnDv + rank * 256);
+            for (int q = 0; q < 32; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+            if (lse != nullptr && own) lse[static_cast<long long>(rr) * kAttnHeads + h] = -INFINITY;
         };
-        // Rescales this thread's half of the lane's O row by f (warp-uniform call).
+        // Rescales this lane's O row by f (warp-uniform call; f = 1 leaves it unchanged).
         auto rescale_o = [&](float f) {
 #pragma unroll 1
-            for (int c0 = 128 * kh; c0 < 128 * kh + 128; c0 += 32) {
+            for (int c0 = 0; c0 < 256; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld32(tmem_base + lane_off + C::TM_O + c0, o);
                 tmem_ld_wait();
@@ -578,12 +551,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t rXR = mapa(sbase + C::OFF_XR, peer);
         float l_peer = 1.f;                           // peer lanes: the denominator received last
         // Peer lanes: takes the rescale factors and denominators that came with the peer's half of
-        // P tile g & 1 (block g, the i-th of the query), rescales this thread's half of those O
-        // rows if told to, and releases the P.V of block g.  Then hands the peer back its half of
-        // the tile of block g - 1 once that block's P.V has completed.
+        // P tile g & 1 (block g, the i-th of the query), rescales these O rows if told to, and
+        // releases the P.V of block g.  Then hands the peer back its half of the tile of block
+        // g - 1 once that block's P.V has completed.
         auto take_p = [&](int g, int i) -> bool {
             const int b = g & 1;
-            if (hl == 0 && lead) mbar_expect_tx(pr_full(b), C::P_TX);
+            if (hl == 0) mbar_expect_tx(pr_full(b), C::P_TX);
             if (!__all_sync(0xffffffffu, wait_bar<true>(pr_full(b), (g >> 1) & 1, timeout_ns, s_abort))) return false;
             const float* mr = reinterpret_cast<const float*>(smem + C::OFF_MR + b * C::MB);
             const float f = mr[hl];
@@ -601,7 +574,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // The tile half and factors of block g - 1 were last read by that block's P.V (its
             // completion is observed here) and by this warp's loads, consumed long before.
             bool w = true;
-            if (g > 0 && hl == 0 && lead) {
+            if (g > 0 && hl == 0) {
                 w = wait_bar(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, timeout_ns, s_abort);
                 if (w) mbar_arrive_cluster_relaxed(mapa(pr_free((g - 1) & 1), peer));
             }
@@ -621,7 +594,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const float inv = 1.f / ep_l;
             const long long orow = (static_cast<long long>(ep_r) * kAttnHeads + h) * kAttnDv + rank * 256;
 #pragma unroll 1
-            for (int c0 = 128 * kh; c0 < 128 * kh + 128; c0 += 32) {
+            for (int c0 = 0; c0 < 256; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld32(tmem_base + lane_off + C::TM_O + c0, o);
                 tmem_ld_wait();
@@ -638,38 +611,40 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
-            if (lse != nullptr && own && lead)
+            if (lse != nullptr && own)
                 lse[static_cast<long long>(ep_r) * kAttnHeads + h] = (ep_m + log2f(ep_l)) * 0.69314718055994530942f;
             tc_fence_before();   // O has been read before the next query's first P.V overwrites it
             ep_r = -1;
             return true;
         };
         while (r < rows && ok) {
-            float m = -INFINITY, l = 0.f;             // own lanes: running max and this half's denominator
+            float m = -INFINITY, l = 0.f;             // own lanes: running max and denominator
             const int g0 = gi;
             for (int i = 0; i < A.nb && ok; ++i) {
                 const int g = g0 + i, b = g & 1;
                 ok = __all_sync(0xffffffffu, wait_bar(s_full(b), (g >> 1) & 1, timeout_ns, s_abort));
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t sraw[32];
-                tmem_ld32(tmem_base + lane_off + C::TM_S + static_cast<uint32_t>(b) * kAttnBK + 32 * kh, sraw);
+                uint32_t sraw[64];
+                const uint32_t ts = tmem_base + lane_off + C::TM_S + static_cast<uint32_t>(b) * kAttnBK;
+                tmem_ld32(ts, *reinterpret_cast<uint32_t(*)[32]>(sraw));
+                tmem_ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(sraw + 32));
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(s_free(b));                // Q.K^T of block g + 2 may overwrite this buffer
                 if (!own) {
                     // ---- peer lanes: send this rank's partial scores of the peer's heads ----
                     if (bulk_pending) bulk_wait_read<0>();   // the previous tile has left XS
-                    named_sync(2, 128);
+                    named_sync(2, 64);
                     uint8_t* xs = smem + C::OFF_XS + hl * 256;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(xs + ((((8 * kh + c) ^ hl) & 15) << 4)) =
+                    for (int c = 0; c < 16; ++c)
+                        *reinterpret_cast<uint4*>(xs + (((c ^ hl) & 15) << 4)) =
                             make_uint4(sraw[4 * c], sraw[4 * c + 1], sraw[4 * c + 2], sraw[4 * c + 3]);
                     fence_proxy_async_smem();
-                    named_sync(2, 128);
+                    named_sync(2, 64);
                     bool sent = true;
-                    if (hl == 0 && lead) {
+                    if (hl == 0) {
                         // the peer has read the previous block's partial scores out of its XR
                         sent = wait_bar<true>(xr_free, (g & 1) ^ 1, timeout_ns, s_abort);
                         if (sent) {
@@ -694,15 +669,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     ok = wait_p_buffer(g) &&
                          __all_sync(0xffffffffu, wait_bar(pcopy_done(b), ((g >> 1) & 1) ^ 1, timeout_ns, s_abort));
                     if (!ok) break;
-                    if (hl == 0 && lead) mbar_expect_tx(xr_full, C::XB);
+                    if (hl == 0) mbar_expect_tx(xr_full, C::XB);
                     ok = __all_sync(0xffffffffu, wait_bar<true>(xr_full, g & 1, timeout_ns, s_abort));
                     if (!ok) break;
-                    float sv[32];
+                    float sv[64];
                     const uint8_t* xr = smem + C::OFF_XR + hl * 256;
                     uint32_t dep = 0;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float4 v = *reinterpret_cast<const float4*>(xr + ((((8 * kh + c) ^ hl) & 15) << 4));
+                    for (int c = 0; c < 16; ++c) {
+                        const float4 v = *reinterpret_cast<const float4*>(xr + (((c ^ hl) & 15) << 4));
                         dep |= __float_as_uint(v.x);
                         sv[4 * c + 0] = __uint_as_float(sraw[4 * c + 0]) + v.x;
                         sv[4 * c + 1] = __uint_as_float(sraw[4 * c + 1]) + v.y;
@@ -712,10 +687,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     // this warp's rows of XR are in registers (each warp load completes for all lanes)
                     if (lane == 0) mbar_arrive_cluster_after(mapa(xr_free, peer), dep);
                     // columns past the last valid entry are masked (identical for every head)
-                    const int nvalid = A.nsel - i * kAttnBK - 32 * kh;
-                    if (nvalid < 32) {
+                    const int nvalid = A.nsel - i * kAttnBK;
+                    if (nvalid < kAttnBK) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
+                        for (int j = 0; j < 64; ++j)
                             if (j >= nvalid) sv[j] = -INFINITY;
                     }
                     // With a positive scale the row maximum is taken on the raw scores and the
@@ -727,22 +702,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                         for (int q = 0; q < 8; ++q) t8[q] = sv[q];
 #pragma unroll
-                        for (int j = 8; j < 32; ++j) t8[j & 7] = fmaxf(t8[j & 7], sv[j]);
+                        for (int j = 8; j < 64; ++j) t8[j & 7] = fmaxf(t8[j & 7], sv[j]);
                         mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
                                    fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
                         mx *= scale_log2;
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
+                        for (int j = 0; j < 64; ++j) {
                             sv[j] = (j < nvalid) ? sv[j] * scale_log2 : -INFINITY;
                             mx = fmaxf(mx, sv[j]);
                         }
                     }
-                    // the block maximum of the head: this half's, combined with the other half's
-                    s_mx[(b * 2 + kh) * kAttnHeads + h] = mx;
-                    ok = pair_sync();
-                    if (!ok) break;
-                    mx = fmaxf(mx, s_mx[(b * 2 + (kh ^ 1)) * kAttnHeads + h]);
                     const float m_new = fmaxf(m, mx);
                     const bool resc = m_new > m + 8.f;       // lazy rescale (always true on the first block)
                     float factor = resc ? fast_exp2(m - m_new) : 1.f;
@@ -754,10 +724,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     // P = 2^(z - m) in bf16 (pairs of keys per 32-bit column); l sums the fp32 values
                     // before rounding, in four independent partial sums
                     const float zs = pos_scale ? scale_log2 : 1.f;
-                    uint32_t pk[16];
+                    uint32_t pk[32];
                     float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < 32; ++j) {
                         const float p0 = fast_exp2(fmaf(sv[2 * j], zs, -m)), p1 = fast_exp2(fmaf(sv[2 * j + 1], zs, -m));
                         const __nv_bfloat162 pr = __floats2bfloat162_rn(p0, p1);
                         ls[j & 3] += p0 + p1;
@@ -766,22 +736,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                     uint8_t* pt = smem + C::OFF_P + b * C::PT + h * 128;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4*>(pt + ((((4 * kh + c) ^ h) & 7) << 4)) =
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(pt + (((c ^ h) & 7) << 4)) =
                             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                     float* ms = reinterpret_cast<float*>(smem + C::OFF_MS + b * C::MB);
-                    if (i == A.nb - 1) {
-                        // last block of the query: the head's denominator is the sum of both halves
-                        // (the peer uses the one sent with the last block)
-                        s_lx[kh * kAttnHeads + h] = l;
-                        ok = pair_sync();
-                        if (!ok) break;
-                        l += s_lx[(kh ^ 1) * kAttnHeads + h];
-                    }
-                    if (lead) {
-                        ms[hl] = factor;
-                        ms[64 + hl] = l;
-                    }
+                    ms[hl] = factor;
+                    ms[64 + hl] = l;
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(p_ready(b));   // the copy warp sends these rows to the peer
