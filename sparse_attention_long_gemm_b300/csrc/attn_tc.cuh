@@ -44,9 +44,11 @@
 // and a small rope buffer, freeing its slots at once, so nearly the whole ring
 // holds gathers in flight: random rows reach about 9 TB/s from L2 only with
 // ~100 KB per SM in flight and with requests of 512 contiguous bytes.  The
-// rest holds the two P tiles (128B-swizzled, K-major), the received partial
-// scores (one tile), the outgoing partial scores (staged once and sent by one
-// bulk copy) and the rescale factors / denominators (two buffers each way).
+// rest holds the two P tiles (128B-swizzled, K-major), two buffers of received
+// partial scores (the peer sends block g + 1 while this rank still works on
+// block g, so the exchange's round trip stays off the softmax's path), a 4 KB
+// staging buffer per sending warp (16 heads per bulk copy) and the rescale
+// factors / denominators (two buffers each way).
 //
 // Per CTA (256 threads; the warp of a role depends on the rank so that the two
 // warps running the softmax have their SM sub-partitions to themselves):
@@ -99,6 +101,7 @@ struct AttnTc {
     static constexpr int QR_HALF = 64 * 64;                         // 64 heads x 32 rope cols = 4 KB
     static constexpr int QR_BYTES = 2 * QR_HALF;
     static constexpr int XB = 64 * kAttnBK * 4;                     // partial scores of 64 heads: 16 KB
+    static constexpr int XSW = 32 * kAttnBK * 4;                    // one peer warp's staging: 32 heads, 8 KB
     static constexpr int PT = kAttnHeads * kAttnBK * 2;             // P tile of 128 heads: 16 KB
     static constexpr int PH = PT / 2;                               // one rank's 64 heads of it
     static constexpr int MB = 64 * 4 * 2;                           // rescale factors + denominators
@@ -106,15 +109,20 @@ struct AttnTc {
     static constexpr int OFF_QR = OFF_RING + kAttnSlots * SLOT;
     static constexpr int OFF_P = OFF_QR + QR_BYTES;                 // [2] P tiles
     static constexpr int OFF_XR = OFF_P + 2 * PT;                   // received partial scores
-    static constexpr int OFF_XS = OFF_XR + XB;                      // outgoing partial scores
-    static constexpr int OFF_MR = OFF_XS + XB;                      // [2] received factors / denominators
+    static constexpr int OFF_XS = OFF_XR + XB;                      // [2 peer warps] outgoing partial scores
+    static constexpr int OFF_MR = OFF_XS + 2 * XSW;                 // [2] received factors / denominators
     static constexpr int OFF_MS = OFF_MR + 2 * MB;                  // [2] outgoing factors / denominators
     static constexpr int OFF_BAR = OFF_MS + 2 * MB;
     // full[S], empty[S], q_tm_full, s_full[2], s_free[2], p_full[2], pv_done[2],
     // xr_full, xr_free, pr_full[2], pr_free[2], done, p_ready[2], pcopy_done[2]
     static constexpr int NBAR = 2 * kAttnSlots + 1 + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 2 + 1 + 2 + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_MISC + 16 + 1024;               // + alignment slack
+    static constexpr int USED = OFF_MISC + 16;
+    // Slack for aligning the dynamic shared memory base to 1024 bytes (the 128B-swizzled
+    // operands need it): whatever the per-CTA limit leaves.  The base is 1024-aligned in
+    // practice; a launch whose base needs more padding reports an error and computes nothing.
+    static constexpr int SLACK = (232448 - USED) < 1024 ? (232448 - USED) : 1024;
+    static constexpr int SMEM = USED + SLACK;
     static constexpr int TMEM_COLS = 512;
     static constexpr int TM_O = 0;
     static constexpr int TM_Q = 256;
@@ -127,7 +135,8 @@ struct AttnTc {
 static_assert(AttnTc::SMEM <= 232448, "attention shared memory exceeds the per-CTA limit");
 static_assert(AttnTc::OFF_P % 1024 == 0, "the P tiles are 128B-swizzled operands (1024-byte atoms)");
 static_assert(2 * AttnTc::QL_TILE + AttnTc::QR_HALF <= AttnTc::SLOT, "a Q item must fit in two slots");
-static_assert(AttnTc::PH % 16 == 0 && AttnTc::MB % 16 == 0 && AttnTc::XB % 16 == 0,
+static_assert(AttnTc::SLACK >= 0, "attention shared memory exceeds the per-CTA limit");
+static_assert(AttnTc::PH % 16 == 0 && AttnTc::MB % 16 == 0 && AttnTc::XB % 16 == 0 && AttnTc::XSW % 16 == 0,
               "bulk copies move multiples of 16 bytes");
 
 // Shared-memory matrix descriptor, 64-byte-swizzled K-major operand
@@ -173,19 +182,18 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Arrive on an mbarrier of the peer CTA without release semantics, once the
-// shared-memory loads that produced `dep` have returned their data: `dep` (any
-// bits of the loaded values, combined by the caller) is folded into the
-// address through an opaque zeroing step, so the arrive cannot issue before
-// those loads complete.  Used to hand back a receive buffer whose contents
-// this warp has read into registers; nothing written before needs ordering.
-__device__ __forceinline__ void mbar_arrive_cluster_after(uint32_t remote_bar, uint32_t dep) {
-    asm volatile("and.b32 %0, %0, 0;" : "+r"(dep));
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar + dep) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+// Relaxed arrive on an mbarrier of the peer CTA that cannot be performed
+// before the shared-memory loads behind `dep` have returned their data.  The
+// caller ORs bits of every loaded value into `dep`; `zero` is 0 at run time
+// but opaque to the compiler (derived from a kernel argument), so the address
+// remote_bar + (dep & zero) truly depends on the loaded registers and the
+// arrive waits for them.  A warp-wide load completes for all of its lanes at
+// once, so one lane's dependency covers the warp's loads of the same
+// instructions.  This hands a receive buffer back to the peer without the
+// cost of a cluster-scope release.
+__device__ __forceinline__ void mbar_arrive_cluster_after(uint32_t remote_bar, uint32_t dep, uint32_t zero) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar + (dep & zero))
+                 : "memory");
 }
 
 // Rows of one query: number of valid selected entries and of 64-key blocks.
@@ -210,6 +218,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     using C = AttnTc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    if (smem - smem_raw > C::SLACK) {   // uniform over the grid: every CTA has the same base
+        if (threadIdx.x == 0) raise_error(DSA_ERR_UNSUPPORTED);
+        return;
+    }
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sRing = sbase + C::OFF_RING, sQR = sbase + C::OFF_QR;
     const uint32_t bar0 = sbase + C::OFF_BAR;
@@ -234,6 +246,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = static_cast<int>(cluster_ctarank());
+    const uint32_t opaque_zero = static_cast<uint32_t>(rows) >> 31;   // rows >= 0: always 0
     const int peer = rank ^ 1;
     const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
     // Warps w and w+4 share an SM sub-partition; the softmax ("own") warps are 0,1 on rank 0
@@ -252,11 +265,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mbar_init(p_full(i), 128);
             mbar_init(pv_done(i), 1);
             mbar_init(pr_full(i), 1);     // a local expect_tx; the peer's bulk copies complete it
-            mbar_init(pr_free(i), 1);     // one arrive from the peer once its P.V of the buffer is done
+            mbar_init(pr_free(i), 1);     // the peer's MMA thread: its P.V of the buffer has completed
             mbar_init(p_ready(i), 2);     // one arrive per own warp: its rows of P and factors are written
             mbar_init(pcopy_done(i), 1);  // the copy warp: this rank's half has been read by its copy
         }
-        mbar_init(xr_full, 1);            // a local expect_tx; the peer's bulk copy completes it
+        mbar_init(xr_full, 1);            // a local expect_tx; the peer's two bulk copies complete it
         mbar_init(xr_free, 2);            // one arrive per own warp of the peer
         mbar_init(done_bar, 1);
         *s_abort = 0;
@@ -387,6 +400,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                 (!first || kk) ? 1u : 0u);
                 tc_commit(pv_done(g & 1));
                 tc_commit(empty(rp_ % kAttnSlots));
+                // the peer's copy of block g + 2 may overwrite this rank's receive buffer g & 1:
+                // this P.V has read its P half, and the factors were read before p_full
+                tc_commit_multicast(pr_free(g & 1), static_cast<uint16_t>(1u << peer));
             };
             for (int r = cl; r < rows && ok; r += ncl) {
                 const AttnRow A = attn_row(rs, r, k);
@@ -552,33 +568,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         float l_peer = 1.f;                           // peer lanes: the denominator received last
         // Peer lanes: takes the rescale factors and denominators that came with the peer's half of
         // P tile g & 1 (block g, the i-th of the query), rescales these O rows if told to, and
-        // releases the P.V of block g.  Then hands the peer back its half of the tile of block
-        // g - 1 once that block's P.V has completed.
-        auto take_p = [&](int g, int i) -> bool {
+        // releases the P.V of block g.  Does nothing and returns false while the peer's half has
+        // not arrived, or while a rescale still has to wait for the P.V of block g - 1.
+        auto try_take = [&](int g, int i) -> bool {
             const int b = g & 1;
-            if (hl == 0) mbar_expect_tx(pr_full(b), C::P_TX);
-            if (!__all_sync(0xffffffffu, wait_bar<true>(pr_full(b), (g >> 1) & 1, timeout_ns, s_abort))) return false;
+            if (!__all_sync(0xffffffffu, mbar_test_cluster(pr_full(b), (g >> 1) & 1))) return false;
             const float* mr = reinterpret_cast<const float*>(smem + C::OFF_MR + b * C::MB);
             const float f = mr[hl];
-            l_peer = mr[64 + hl];
             if (i > 0 && __any_sync(0xffffffffu, f != 1.f)) {
-                // O must hold every earlier P.V before it is rescaled
-                if (!__all_sync(0xffffffffu, wait_bar(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, timeout_ns, s_abort)))
-                    return false;
+                // O must hold every earlier P.V before it is rescaled.  (The peer sent block g
+                // after this rank's P.V of block g - 2 completed, so the phase tested is current.)
+                if (!__all_sync(0xffffffffu, mbar_test(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1))) return false;
                 tc_fence_after();
                 rescale_o(f);
                 tmem_st_wait();
             }
+            l_peer = mr[64 + hl];
             tc_fence_before();
             mbar_arrive(p_full(b));
-            // The tile half and factors of block g - 1 were last read by that block's P.V (its
-            // completion is observed here) and by this warp's loads, consumed long before.
-            bool w = true;
-            if (g > 0 && hl == 0) {
-                w = wait_bar(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, timeout_ns, s_abort);
-                if (w) mbar_arrive_cluster_relaxed(mapa(pr_free((g - 1) & 1), peer));
-            }
-            return __all_sync(0xffffffffu, w);
+            return true;
         };
         // The output epilogue of a finished query is deferred until this lane has read S of the
         // next query's first block (and, for peer lanes, sent its partial scores): the first
@@ -620,7 +628,78 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         while (r < rows && ok) {
             float m = -INFINITY, l = 0.f;             // own lanes: running max and denominator
             const int g0 = gi;
-            for (int i = 0; i < A.nb && ok; ++i) {
+            if (!own) {
+                // ---- peer lanes: send this rank's partial scores of the peer's heads as soon as a
+                // block's scores are in and the peer's receive buffer is free, and take the peer's
+                // P whenever it has arrived.  Every condition is tested without blocking, so neither
+                // stream waits behind the other and neither peer warp waits for its sibling (each
+                // stages and sends its own 32 rows). ----
+                const int pwi = hl >> 5;
+                const uint32_t sxs = sbase + C::OFF_XS + static_cast<uint32_t>(pwi * C::XSW);
+                uint8_t* xs = smem + C::OFF_XS + pwi * C::XSW + lane * 256;
+                int ns = 0, nt = 0, nt_posted = -1;
+                uint64_t t_idle = 0;
+                while (ok && nt < A.nb) {
+                    bool prog = false;
+                    if (ns < A.nb) {
+                        const int g = g0 + ns, b = g & 1;
+                        // S of block g is in, and the peer has read block g - 1 out of its buffer
+                        if (__all_sync(0xffffffffu, mbar_test(s_full(b), (g >> 1) & 1) &&
+                                                         mbar_test_cluster(xr_free, (g & 1) ^ 1))) {
+                            tc_fence_after();
+                            uint32_t sraw[64];
+                            const uint32_t ts = tmem_base + lane_off + C::TM_S + static_cast<uint32_t>(b) * kAttnBK;
+                            tmem_ld32(ts, *reinterpret_cast<uint32_t(*)[32]>(sraw));
+                            tmem_ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(sraw + 32));
+                            tmem_ld_wait();
+                            tc_fence_before();
+                            mbar_arrive(s_free(b));            // Q.K^T of block g + 2 may overwrite this buffer
+                            if (lane == 0 && bulk_pending) bulk_wait_read<0>();   // the staging buffer is free
+                            __syncwarp();
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                *reinterpret_cast<uint4*>(xs + (((c ^ hl) & 15) << 4)) =
+                                    make_uint4(sraw[4 * c], sraw[4 * c + 1], sraw[4 * c + 2], sraw[4 * c + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                bulk_copy_to_peer(rXR + static_cast<uint32_t>(pwi * C::XSW), sxs, C::XSW,
+                                                  mapa(xr_full, peer));
+                                bulk_commit();
+                                bulk_pending = 1;
+                            }
+                            ++ns;
+                            prog = true;
+                            if (ns == 1) ok = run_epilogue();   // the previous query's output
+                        }
+                    }
+                    if (ok && !prog && nt < ns) {
+                        if (nt_posted != nt) {   // once per block, after the buffer's previous phase
+                            if (hl == 0) mbar_expect_tx(pr_full((g0 + nt) & 1), C::P_TX);
+                            nt_posted = nt;
+                        }
+                        if (try_take(g0 + nt, nt)) {
+                            ++nt;
+                            prog = true;
+                        }
+                    }
+                    if (prog) {
+                        t_idle = 0;
+                    } else {
+                        const uint64_t now = global_ns();
+                        if (t_idle == 0) {
+                            t_idle = now;
+                        } else if (now - t_idle > timeout_ns) {
+                            *s_abort = 1;
+                            raise_error(DSA_ERR_TIMEOUT);
+                            ok = false;
+                        } else if (*s_abort) {
+                            ok = false;
+                        }
+                    }
+                }
+            }
+            for (int i = 0; i < A.nb && ok && own; ++i) {
                 const int g = g0 + i, b = g & 1;
                 ok = __all_sync(0xffffffffu, wait_bar(s_full(b), (g >> 1) & 1, timeout_ns, s_abort));
                 if (!ok) break;
@@ -632,33 +711,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(s_free(b));                // Q.K^T of block g + 2 may overwrite this buffer
-                if (!own) {
-                    // ---- peer lanes: send this rank's partial scores of the peer's heads ----
-                    if (bulk_pending) bulk_wait_read<0>();   // the previous tile has left XS
-                    named_sync(2, 64);
-                    uint8_t* xs = smem + C::OFF_XS + hl * 256;
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        *reinterpret_cast<uint4*>(xs + (((c ^ hl) & 15) << 4)) =
-                            make_uint4(sraw[4 * c], sraw[4 * c + 1], sraw[4 * c + 2], sraw[4 * c + 3]);
-                    fence_proxy_async_smem();
-                    named_sync(2, 64);
-                    bool sent = true;
-                    if (hl == 0) {
-                        // the peer has read the previous block's partial scores out of its XR
-                        sent = wait_bar<true>(xr_free, (g & 1) ^ 1, timeout_ns, s_abort);
-                        if (sent) {
-                            bulk_copy_to_peer(rXR, sbase + C::OFF_XS, C::XB, mapa(xr_full, peer));
-                            bulk_commit();
-                            bulk_pending = 1;
-                        }
-                    }
-                    ok = __all_sync(0xffffffffu, sent);
-                    if (ok && i == 0) ok = run_epilogue();   // the previous query's output
-                    // ---- then take the peer's P of the PREVIOUS block, so that sending never
-                    // waits for receiving ----
-                    if (ok && i > 0) ok = take_p(g - 1, i - 1);
-                } else {
+                {
                     // ---- own lanes: complete the scores, softmax, write P for both ranks ----
                     if (i == 0) {
                         ok = run_epilogue();           // the previous query's output
@@ -684,8 +737,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         sv[4 * c + 2] = __uint_as_float(sraw[4 * c + 2]) + v.z;
                         sv[4 * c + 3] = __uint_as_float(sraw[4 * c + 3]) + v.w;
                     }
-                    // this warp's rows of XR are in registers (each warp load completes for all lanes)
-                    if (lane == 0) mbar_arrive_cluster_after(mapa(xr_free, peer), dep);
+                    // Hand XR back to the peer, whose next bulk copy overwrites it, once this
+                    // warp's loads of it have returned (a zeroing step the compiler could fold
+                    // let the arrive overtake them, and the peer overwrite the first rows).
+                    if (lane == 0) mbar_arrive_cluster_after(mapa(xr_free, peer), dep, opaque_zero);
                     // columns past the last valid entry are masked (identical for every head)
                     const int nvalid = A.nsel - i * kAttnBK;
                     if (nvalid < kAttnBK) {
@@ -757,7 +812,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     mbar_arrive(p_full(b));
                 }
             }
-            if (ok && !own) ok = take_p(g0 + A.nb - 1, A.nb - 1);
             if (!ok) break;
             gi = g0 + A.nb;
             rp += A.nb;
