@@ -637,15 +637,38 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const int pwi = hl >> 5;
                 const uint32_t sxs = sbase + C::OFF_XS + static_cast<uint32_t>(pwi * C::XSW);
                 uint8_t* xs = smem + C::OFF_XS + pwi * C::XSW + lane * 256;
-                int ns = 0, nt = 0, nt_posted = -1;
+                int ns = 0, nst = 0, nt = 0, nt_posted = -1;   // blocks sent, staged, taken
                 uint64_t t_idle = 0;
                 while (ok && nt < A.nb) {
                     bool prog = false;
-                    if (ns < A.nb) {
-                        const int g = g0 + ns, b = g & 1;
-                        // S of block g is in, and the peer has read block g - 1 out of its buffer
-                        if (__all_sync(0xffffffffu, mbar_test(s_full(b), (g >> 1) & 1) &&
-                                                         mbar_test_cluster(xr_free, (g & 1) ^ 1))) {
+                    // a staged block goes out as soon as the peer has read the previous one
+                    if (nst > ns && __all_sync(0xffffffffu, mbar_test_cluster(xr_free, ((g0 + ns) & 1) ^ 1))) {
+                        if (lane == 0) {
+                            bulk_copy_to_peer(rXR + static_cast<uint32_t>(pwi * C::XSW), sxs, C::XSW,
+                                              mapa(xr_full, peer));
+                            bulk_commit();
+                            bulk_pending = 1;
+                        }
+                        ++ns;
+                        prog = true;
+                        if (ns == 1) ok = run_epilogue();   // the previous query's output
+                    }
+                    if (ok && !prog && nt < ns) {
+                        if (nt_posted != nt) {   // once per block, after the buffer's previous phase
+                            if (hl == 0) mbar_expect_tx(pr_full((g0 + nt) & 1), C::P_TX);
+                            nt_posted = nt;
+                        }
+                        if (try_take(g0 + nt, nt)) {
+                            ++nt;
+                            prog = true;
+                        }
+                    }
+                    // otherwise the next block is staged once its S is in, so that only the copy
+                    // waits for the peer's buffer (staging may wait for the previous copy to have
+                    // read the staging buffer, so it comes after the takes)
+                    if (!prog && nst == ns && nst < A.nb) {
+                        const int g = g0 + nst, b = g & 1;
+                        if (__all_sync(0xffffffffu, mbar_test(s_full(b), (g >> 1) & 1))) {
                             tc_fence_after();
                             uint32_t sraw[64];
                             const uint32_t ts = tmem_base + lane_off + C::TM_S + static_cast<uint32_t>(b) * kAttnBK;
@@ -662,24 +685,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                     make_uint4(sraw[4 * c], sraw[4 * c + 1], sraw[4 * c + 2], sraw[4 * c + 3]);
                             fence_proxy_async_smem();
                             __syncwarp();
-                            if (lane == 0) {
-                                bulk_copy_to_peer(rXR + static_cast<uint32_t>(pwi * C::XSW), sxs, C::XSW,
-                                                  mapa(xr_full, peer));
-                                bulk_commit();
-                                bulk_pending = 1;
-                            }
-                            ++ns;
-                            prog = true;
-                            if (ns == 1) ok = run_epilogue();   // the previous query's output
-                        }
-                    }
-                    if (ok && !prog && nt < ns) {
-                        if (nt_posted != nt) {   // once per block, after the buffer's previous phase
-                            if (hl == 0) mbar_expect_tx(pr_full((g0 + nt) & 1), C::P_TX);
-                            nt_posted = nt;
-                        }
-                        if (try_take(g0 + nt, nt)) {
-                            ++nt;
+                            ++nst;
                             prog = true;
                         }
                     }
