@@ -193,7 +193,9 @@ topk_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int k, i
 //   4. emit: the selected positions are marked in an n-bit bitmap, so one scan
 //      of its words (a block prefix sum of their bit counts) writes them in
 //      ascending order; a second bitmap holds the keys equal to the k-th when
-//      only some of them are kept (the lowest positions).
+//      only some of them are kept (the lowest positions).  The positions are
+//      staged in the (by then unused) candidate list and leave in coalesced
+//      16-byte stores.
 // When the candidates are fewer than k (the sample's rank-rho key lay above
 // the row's k-th score) or overflow a warp's part of the list (heavy ties, or
 // high scores bunched in one warp's groups), the row runs the exact full-row
@@ -376,6 +378,8 @@ topk_rows_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int
     uint32_t* eqb = gtb + bw;
     uint32_t* hist = gtb;                          // 2048 bins over both bitmaps (bw >= 1024)
     uint32_t* skey = reinterpret_cast<uint32_t*>(cand);   // sample keys (before the filter)
+    int* stage = reinterpret_cast<int*>(cand);            // the emitted positions (after the select)
+    const bool staged = k <= 2 * kTkCap;
     const uint32_t s_samp = smem_u32(tk_smem + TkSmem::OFF_SAMP);
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const uint32_t lt = (1u << lane) - 1u;
@@ -716,8 +720,20 @@ topk_rows_kernel(RowSpec rs, const float* __restrict__ scores, long long ld, int
                 while (sel) {
                     const int b = __ffs(sel) - 1;
                     sel &= sel - 1;
-                    if (slot < static_cast<uint32_t>(k)) out[slot] = 32 * w + b;   // exactly k are marked;
-                    ++slot;                                                          // this only bounds writes
+                    if (slot < static_cast<uint32_t>(k)) {   // exactly k are marked; this only bounds writes
+                        if (staged) stage[slot] = 32 * w + b;
+                        else out[slot] = 32 * w + b;
+                    }
+                    ++slot;
+                }
+            }
+            if (staged) {   // the row's k positions leave shared memory in coalesced stores
+                __syncthreads();
+                if ((k & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+                    for (int i = tid; i < (k >> 2); i += kTkThreads)
+                        reinterpret_cast<int4*>(out)[i] = reinterpret_cast<const int4*>(stage)[i];
+                } else {
+                    for (int i = tid; i < k; i += kTkThreads) out[i] = stage[i];
                 }
             }
         }
