@@ -9,6 +9,9 @@ from .dsa_oracle import (  # noqa: F401
     dsa_prefill,
     index_scores,
     index_scores_row,
+    indexer_inputs,
+    linear,
     masked_attention_row,
     topk_select,
+    update_indexer,
 )

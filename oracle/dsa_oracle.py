@@ -369,3 +369,55 @@ def dsa_decode(q_idx, w, q, idx_cache, kv_cache, cache_seqlens, topk, scale, d_v
         "out": res_out,
         "lse": res_lse,
     }
+
+
+# ---------------------------------------------------------------------------
+# Upstream of the path: the indexer's inputs and its key-cache update
+# ---------------------------------------------------------------------------
+def linear(x, weight):
+    """y = x . weight^T for x [..., K] and weight [N, K] (a bias-free projection, the form of
+    every projection the "DeepSeek-V3.2" page names for the indexer); float64."""
+    return _f64(x) @ _f64(weight).T
+
+
+def indexer_inputs(q_latent, x, wq_b, wk, w_proj, n_heads, head_dim):
+    """The Lightning Indexer's inputs ("DeepSeek-V3.2" page, section "DeepSeek Sparse Attention
+    (DSA)"): the indexer scores queries taken from the MLA query latent
+    q_latent = q_a_layernorm(q_a_proj(x)) through its projection wq_b (sized by q_lora_rank);
+    its head weights come from the weights_proj module; its single-head key of index_head_dim
+    per token comes from a key projection of the hidden state x.  The page gives no further
+    detail, so each is read as a plain bias-free linear map:
+
+        q_I[t] = reshape(wq_b . q_latent[t], [n_heads, head_dim])
+        k_I[t] = wk . x[t]
+        w[t]   = w_proj . x[t]
+
+    q_latent [T, q_lora_rank], x [T, hidden], wq_b [n_heads * head_dim, q_lora_rank],
+    wk [head_dim, hidden], w_proj [n_heads, hidden] -> (q_I [T, n_heads, head_dim],
+    k_I [T, head_dim], w [T, n_heads]), float64."""
+    T = _f64(q_latent).shape[0]
+    q_i = linear(q_latent, wq_b).reshape(T, n_heads, head_dim)
+    return q_i, linear(x, wk), linear(x, w_proj)
+
+
+def update_indexer(idx_cache, kv_cache, cache_seqlens, k_new, kv_new):
+    """The decode step's cache update ("DeepSeek-V3.2" page, DSA section: the indexer keeps its
+    own per-token key cache next to the K/V cache and updates it through update_indexer()).
+    For every sequence b with room left, the new token's indexer key k_new[b] and latent row
+    kv_new[b] are written at position cache_seqlens[b] of idx_cache[b] and kv_cache[b], and
+    the length grows by one; a full cache is left as it is.  Returns new arrays
+    (idx_cache, kv_cache, cache_seqlens, full) with `full` marking the sequences that had no
+    room; the values are copied, not converted."""
+    idx = np.array(idx_cache, copy=True)
+    kv = np.array(kv_cache, copy=True)
+    lens = np.array(cache_seqlens, copy=True)
+    full = np.zeros(len(lens), dtype=bool)
+    for b in range(len(lens)):
+        p = int(lens[b])
+        if p >= idx.shape[1]:
+            full[b] = True
+            continue
+        idx[b, p] = k_new[b]
+        kv[b, p] = kv_new[b]
+        lens[b] = p + 1
+    return idx, kv, lens, full
