@@ -723,6 +723,101 @@ def cpu_baseline(cfg, args):
                       f"{dt:.1f} s of CPU work"}
 
 
+Q_LORA_RANK = 1536    # DeepseekV3Config defaults (q_lora_rank, hidden_size), shared by V3.2
+HIDDEN = 7168
+
+
+def run_inputs(args, cfg):
+    """Upstream of the path: the indexer's input projections for every token of the prefill
+    workload (q_idx = q_latent . wq_b^T, k_idx = x . wk^T, w = x . w_proj^T) on the tensor cores,
+    and one update_indexer append per sequence of the decode workload.  One JSON line, its own
+    metric (the projections' TFLOP/s against the bf16 peak); not the step of the headline."""
+    import torch
+
+    import sparse_attention_long_gemm_b300 as dsa
+    from sparse_attention_long_gemm_b300.synth import CONFIGS
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    p = dsa.params_from_config(cfg)
+    T, H, D = sum(cfg.seqlens), cfg.n_idx_heads, cfg.idx_dim
+    g = torch.Generator(device=dev).manual_seed(0)
+    q_lat = torch.randn(T, Q_LORA_RANK, device=dev, generator=g).to(torch.bfloat16)
+    x = torch.randn(T, HIDDEN, device=dev, generator=g).to(torch.bfloat16)
+    wq_b = (torch.randn(H * D, Q_LORA_RANK, device=dev, generator=g) / Q_LORA_RANK ** 0.5).to(torch.bfloat16)
+    wk = (torch.randn(D, HIDDEN, device=dev, generator=g) / HIDDEN ** 0.5).to(torch.bfloat16)
+    wp = (torch.randn(H, HIDDEN, device=dev, generator=g) / HIDDEN ** 0.5).to(torch.bfloat16)
+    q_idx = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    k_idx = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+    w = torch.empty((T, H), dtype=torch.float32, device=dev)
+    # decode caches of the decode workload, one append per sequence
+    dc = CONFIGS["decode"]
+    Bn, M = dc.batch, dc.max_ctx
+    idx_cache = torch.zeros((Bn, M, D), dtype=torch.bfloat16, device=dev)
+    kv_cache = torch.zeros((Bn, M, dc.d_qk), dtype=torch.bfloat16, device=dev)
+    k_new = torch.randn(Bn, D, device=dev, generator=g).to(torch.bfloat16)
+    kv_new = torch.randn(Bn, dc.d_qk, device=dev, generator=g).to(torch.bfloat16)
+    lens = torch.zeros(Bn, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    shapes = [(q_lat, Q_LORA_RANK, wq_b, H * D, q_idx, dsa.DSA_BF16), (x, HIDDEN, wk, D, k_idx, dsa.DSA_BF16),
+              (x, HIDDEN, wp, H, w, dsa.DSA_FP32)]
+
+    def step(evs=None):
+        for i, (a, kk, b, n, c, dt) in enumerate(shapes):
+            if evs is not None:
+                evs[i].record()
+            dsa.dsa_gemm_bf16(a, kk, b, kk, T, n, kk, c, n, dt)
+        if evs is not None:
+            evs[3].record()
+        lens.zero_()
+        dsa.dsa_update_indexer(p, k_new, kv_new, Bn, M, lens, idx_cache, kv_cache)
+        if evs is not None:
+            evs[4].record()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks_dir = os.environ.get("DSA_CLOCKS_DIR") or tempfile.gettempdir()
+    sampler = ClockSampler(0, os.path.join(clocks_dir, "dsa_clocks_inputs.csv"))
+    torch.cuda.synchronize(dev)
+    for s_ in range(args.steps):
+        flush.zero_()
+        step(evs[s_])
+    torch.cuda.synchronize(dev)
+    st = [[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs]
+    extra = clock_tail(step, flush, dev, [sum(x) for x in st])
+    clocks = sampler.stop()
+    if clocks is not None:
+        clocks["untimed_steps_after"] = extra
+    if dsa.dsa_get_device_error() != 0:
+        raise RuntimeError("device error during timing")
+    ms = [statistics.median(x[i] for x in st) for i in range(4)]
+    peaks = _peaks()
+    flops = [2.0 * T * kk * n for (_, kk, _, n, _, _) in shapes]
+    tf = [f / (m * 1e9) for f, m in zip(flops, ms[:3])]
+    tot_tf = sum(flops) / (sum(ms[:3]) * 1e9)
+    upd_bytes = 2 * Bn * (D + dc.d_qk) * 2 + 2 * Bn * 4   # rows read and written, lengths read and written
+    upd_gbs = upd_bytes / (ms[3] * 1e6)
+    names = ["q_idx = q_latent.wq_b^T", "k_idx = x.wk^T", "w = x.w_proj^T"]
+    line = {
+        "metric": "indexer input projections TFLOP/s (q_lora_rank 1536, hidden 7168)",
+        "value": tot_tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sum(ms[:3]), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: {T} tokens; update_indexer: {Bn} sequences of the decode caches",
+                   "l2": "flushed (256 MB write) between timed steps", "timing": f"median of {args.steps} steps"},
+        "stages": {nm: {"m": T, "n": n, "k": kk, "ms": m, "tflops": t, "frac_of_peak": t / peaks["bf16_tflops"]}
+                   for nm, (_, kk, _, n, _, _), m, t in zip(names, shapes, ms[:3], tf)},
+        "update_indexer": {"us": ms[3] * 1e3, "bytes": upd_bytes, "gbs": upd_gbs},
+        "roofline": {"bound": "tensor", "kernel": "gemm_tc_kernel<256,true>", "achieved": tf[0],
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": tf[0] / peaks["bf16_tflops"],
+                     "peak_kind": f"bf16 dense, burst, {peaks['source']}"},
+        "clocks": clocks, "gpu_launches": 4,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -733,6 +828,8 @@ def main():
     ap.add_argument("--seqlen", type=int, default=0, help="override: one prefill sequence of this length")
     ap.add_argument("--indexer", default="native", choices=["native", "fp8"],
                     help="fp8: the indexer's FP8 form (rotation + E4M3 codes) in place of bf16")
+    ap.add_argument("--stage", default="forward", choices=["forward", "inputs"],
+                    help="inputs: time the indexer's input projections and the cache append instead")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=24)
@@ -747,7 +844,9 @@ def main():
         from sparse_attention_long_gemm_b300.synth import scaled
 
         cfg = scaled(cfg, seqlens=(args.seqlen,), varlen_range=())
-    if args.impl == "reference":
+    if args.stage == "inputs":
+        run_inputs(args, cfg)
+    elif args.impl == "reference":
         run_reference(args, cfg)
     else:
         run_ours(args, cfg)

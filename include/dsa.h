@@ -225,6 +225,50 @@ int dsa_index_scores_fp8_decode(const dsa_params* params, const void* q8, const 
                                 const int* cache_seqlens, int batch, int max_ctx,
                                 float* scores, long long ld, void* stream);
 
+/* ---- Upstream of the path: the indexer's inputs and its key-cache update ----
+ * DeepSeek-V3.2 page, "DeepSeek Sparse Attention (DSA)": the indexer scores
+ * queries taken from the MLA query latent q_latent = q_a_layernorm(q_a_proj(x))
+ * through its projection wq_b (sized by q_lora_rank), weights its heads with the
+ * weights_proj module, and keeps its own single-head key cache of index_head_dim
+ * per token, updated through update_indexer().  The page gives no further form,
+ * so every projection is a bias-free linear map.
+ *
+ * dsa_gemm_bf16: C[m, n] = A[m, k] . B[n, k]^T on the tensor cores, bf16
+ *   operands with k contiguous (rows lda / ldb elements apart), fp32
+ *   accumulation, C [m, n] (rows ldc apart) written as c_dtype (DSA_BF16 rounds
+ *   to nearest even, DSA_FP32 as accumulated).  Device pointers, 16-byte
+ *   aligned; lda, ldb multiples of 8; ldc a multiple of 8 (bf16) or 4 (fp32).
+ *   Errors: DSA_ERR_ARG (null pointer, a size < 1, bad c_dtype), DSA_ERR_SHAPE
+ *   (a leading dimension too small or misaligned, a misaligned pointer),
+ *   DSA_ERR_UNSUPPORTED (m > 65535 * 128).
+ * dsa_indexer_inputs: for T = total_q tokens (bf16 params only),
+ *   q_idx [T, H_I, D_I] = q_latent [T, q_lora_rank] . wq_b^T  (wq_b [H_I*D_I, q_lora_rank]),
+ *   k_idx [T, D_I]      = x [T, hidden] . wk^T              (wk [D_I, hidden]),
+ *   w [T, H_I] (fp32)   = x . w_proj^T                      (w_proj [H_I, hidden]),
+ *   the inputs dsa_index_scores and dsa_forward read.  All bf16 except w;
+ *   q_lora_rank, hidden, D_I multiples of 8, H_I a multiple of 4.  total_q = 0
+ *   does nothing.  Errors: those of dsa_gemm_bf16, DSA_ERR_UNSUPPORTED for an
+ *   fp32 params.
+ * dsa_update_indexer: the decode step's append.  For every sequence b the new
+ *   token's indexer key k_new [batch, D_I] and latent row kv_new [batch, d_qk]
+ *   (params->dtype) are written at position cache_seqlens[b] of idx_cache
+ *   [batch, max_ctx, D_I] and kv_cache [batch, max_ctx, d_qk], then
+ *   cache_seqlens[b] (device memory, read and written by the call) grows by
+ *   one.  A sequence whose cache is full (cache_seqlens[b] >= max_ctx) or whose
+ *   length is negative is left untouched and raises DSA_ERR_DEVICE_DATA in the
+ *   device error word.  Rows must be multiples of 16 bytes and the arrays
+ *   16-byte aligned (DSA_ERR_SHAPE / DSA_ERR_ARG otherwise).  The caches are
+ *   the dense layout the decode calls read. */
+int dsa_gemm_bf16(const void* a, long long lda, const void* b, long long ldb, int m, int n, int k,
+                  void* c, long long ldc, int c_dtype, void* stream);
+int dsa_indexer_inputs(const dsa_params* params, const void* q_latent, const void* x,
+                       const void* wq_b, const void* wk, const void* w_proj, int total_q,
+                       int q_lora_rank, int hidden, void* q_idx, void* k_idx, float* w,
+                       void* stream);
+int dsa_update_indexer(const dsa_params* params, const void* k_new, const void* kv_new, int batch,
+                       int max_ctx, int* cache_seqlens, void* idx_cache, void* kv_cache,
+                       void* stream);
+
 /* Synchronises `stream`, then returns and clears the device error word:
  * DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_DATA (DSA_ERR_CUDA if the
  * synchronisation itself failed). */

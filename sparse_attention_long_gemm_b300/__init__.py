@@ -21,11 +21,13 @@ from ._binding import (  # noqa: F401
     dsa_decode_workspace_size,
     dsa_forward,
     dsa_forward_decode,
+    dsa_gemm_bf16,
     dsa_get_device_error,
     dsa_index_scores,
     dsa_index_scores_decode,
     dsa_index_scores_fp8,
     dsa_index_scores_fp8_decode,
+    dsa_indexer_inputs,
     dsa_indexer_quantize_fp8,
     dsa_path_name,
     dsa_selftest_wait_timeout,
@@ -34,10 +36,26 @@ from ._binding import (  # noqa: F401
     dsa_sparse_mla_attn_decode,
     dsa_topk,
     dsa_topk_decode,
+    dsa_update_indexer,
     dsa_workspace_size,
     make_params,
     params_from_config,
 )
+
+
+def indexer_inputs(p, q_latent, x, wq_b, wk, w_proj, stream=None):
+    """The indexer's inputs from the query latent [T, q_lora_rank] and the hidden state
+    [T, hidden] (bf16): (q_idx [T, H_I, D_I] bf16, k_idx [T, D_I] bf16, w [T, H_I] fp32)."""
+    import torch
+
+    T, R = q_latent.shape
+    E = x.shape[1]
+    H, D = p.n_idx_heads, p.idx_dim
+    q_idx = torch.empty((T, H, D), dtype=torch.bfloat16, device=x.device)
+    k_idx = torch.empty((T, D), dtype=torch.bfloat16, device=x.device)
+    w = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    dsa_indexer_inputs(p, q_latent, x, wq_b, wk, w_proj, T, R, E, q_idx, k_idx, w, stream)
+    return q_idx, k_idx, w
 
 
 def _round4(x):

@@ -46,6 +46,9 @@ EXPORTED = [
     "dsa_indexer_quantize_fp8",
     "dsa_index_scores_fp8",
     "dsa_index_scores_fp8_decode",
+    "dsa_gemm_bf16",
+    "dsa_indexer_inputs",
+    "dsa_update_indexer",
 ]
 
 
@@ -115,6 +118,12 @@ def lib():
         L.dsa_index_scores_fp8.argtypes = [P, vp, vp, vp, vp, vp, i, i, i, vp, ll, vp]
         L.dsa_index_scores_fp8_decode.restype = i
         L.dsa_index_scores_fp8_decode.argtypes = [P, vp, vp, vp, vp, vp, i, i, vp, ll, vp]
+        L.dsa_gemm_bf16.restype = i
+        L.dsa_gemm_bf16.argtypes = [vp, ll, vp, ll, i, i, i, vp, ll, i, vp]
+        L.dsa_indexer_inputs.restype = i
+        L.dsa_indexer_inputs.argtypes = [P, vp, vp, vp, vp, vp, i, i, i, vp, vp, vp, vp]
+        L.dsa_update_indexer.restype = i
+        L.dsa_update_indexer.argtypes = [P, vp, vp, i, i, vp, vp, vp, vp]
         L.dsa_get_device_error.restype = i
         L.dsa_get_device_error.argtypes = [vp]
         L.dsa_set_wait_timeout_ns.restype = ll
@@ -251,6 +260,23 @@ def dsa_index_scores_fp8_decode(p, q8, wq, k8_cache, ksc_cache, cache_seqlens, b
     rc = lib().dsa_index_scores_fp8_decode(ctypes.byref(p), _ptr(q8), _ptr(wq), _ptr(k8_cache), _ptr(ksc_cache),
                                            _ptr(cache_seqlens), batch, max_ctx, _ptr(scores), ld, _stream(stream))
     _check(rc, "dsa_index_scores_fp8_decode")
+
+
+def dsa_gemm_bf16(a, lda, b, ldb, m, n, k, c, ldc, c_dtype, stream=None):
+    rc = lib().dsa_gemm_bf16(_ptr(a), lda, _ptr(b), ldb, m, n, k, _ptr(c), ldc, c_dtype, _stream(stream))
+    _check(rc, "dsa_gemm_bf16")
+
+
+def dsa_indexer_inputs(p, q_latent, x, wq_b, wk, w_proj, total_q, q_lora_rank, hidden, q_idx, k_idx, w, stream=None):
+    rc = lib().dsa_indexer_inputs(ctypes.byref(p), _ptr(q_latent), _ptr(x), _ptr(wq_b), _ptr(wk), _ptr(w_proj),
+                                  total_q, q_lora_rank, hidden, _ptr(q_idx), _ptr(k_idx), _ptr(w), _stream(stream))
+    _check(rc, "dsa_indexer_inputs")
+
+
+def dsa_update_indexer(p, k_new, kv_new, batch, max_ctx, cache_seqlens, idx_cache, kv_cache, stream=None):
+    rc = lib().dsa_update_indexer(ctypes.byref(p), _ptr(k_new), _ptr(kv_new), batch, max_ctx, _ptr(cache_seqlens),
+                                  _ptr(idx_cache), _ptr(kv_cache), _stream(stream))
+    _check(rc, "dsa_update_indexer")
 
 
 def dsa_get_device_error(stream=None) -> int:

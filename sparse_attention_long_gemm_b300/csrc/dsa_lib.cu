@@ -16,6 +16,7 @@
 
 #include "attn_simt.cuh"
 #include "attn_tc.cuh"
+#include "gemm_tc.cuh"
 #include "indexer_fp8.cuh"
 #include "indexer_simt.cuh"
 #include "indexer_tc.cuh"
@@ -96,6 +97,12 @@ int device_info(DevInfo** out) {
         set(reinterpret_cast<const void*>(&indexer_tc_kernel<kDecNQ, kF8DecKS, kDecQB, true>),
             IdxTc<kDecNQ, kF8DecKS, kDecQB, true>::SMEM);
         set(reinterpret_cast<const void*>(&attn_tc_kernel), AttnTc::SMEM);
+        set(reinterpret_cast<const void*>(&gemm_tc_kernel<64, true>), GemmTc<64>::SMEM);
+        set(reinterpret_cast<const void*>(&gemm_tc_kernel<128, true>), GemmTc<128>::SMEM);
+        set(reinterpret_cast<const void*>(&gemm_tc_kernel<256, true>), GemmTc<256>::SMEM);
+        set(reinterpret_cast<const void*>(&gemm_tc_kernel<64, false>), GemmTc<64>::SMEM);
+        set(reinterpret_cast<const void*>(&gemm_tc_kernel<128, false>), GemmTc<128>::SMEM);
+        set(reinterpret_cast<const void*>(&gemm_tc_kernel<256, false>), GemmTc<256>::SMEM);
         set(reinterpret_cast<const void*>(&topk_rows_kernel), TkSmem::bytes(kTkMaxLen));
         set(reinterpret_cast<const void*>(&indexer_simt_kernel<float>), indexer_simt_smem(128, 128));
         set(reinterpret_cast<const void*>(&indexer_simt_kernel<__nv_bfloat16>), indexer_simt_smem(128, 128));
@@ -139,6 +146,20 @@ int make_tmap_bf16(CUtensorMap* tm, const void* base, long long rows, long long 
     return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_CUDA;
 }
 
+// 2-D bf16 tensor [rows, cols] with rows `ld` elements apart, box [box_rows, 64], 128-byte swizzle.
+int make_tmap_bf16_ld(CUtensorMap* tm, const void* base, long long rows, long long cols, long long ld, int box_rows) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return DSA_ERR_CUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_CUDA;
+}
+
 // 2-D uint8 tensor [rows, cols] (E4M3 codes), box [box_rows, 128 bytes], 128-byte swizzle.
 int make_tmap_u8(CUtensorMap* tm, const void* base, long long rows, long long cols, int box_rows) {
     auto fn = encode_fn();
@@ -156,6 +177,29 @@ int make_tmap_u8(CUtensorMap* tm, const void* base, long long rows, long long co
 // ---------------------------------------------------------------------------
 // stage launchers (arguments already validated)
 // ---------------------------------------------------------------------------
+// C[M, N] = A[M, K] . B[N, K]^T: a tile width that the output columns fill
+int run_gemm(const void* a, long long lda, const void* b, long long ldb, int m, int n, int k, void* c, long long ldc,
+             bool out_bf16, cudaStream_t st) {
+    DevInfo* di = nullptr;
+    int rc = device_info(&di);
+    if (rc != DSA_OK) return rc;
+    const int bn = n >= 256 ? 256 : (n > 64 ? 128 : 64);
+    CUtensorMap ta, tb;
+    if ((rc = make_tmap_bf16_ld(&ta, a, m, k, lda, kGemmBM)) != DSA_OK) return rc;
+    if ((rc = make_tmap_bf16_ld(&tb, b, n, k, ldb, bn)) != DSA_OK) return rc;
+    const dim3 grid((n + bn - 1) / bn, (m + kGemmBM - 1) / kGemmBM);
+    const unsigned long long to = static_cast<unsigned long long>(g_timeout_ns.load());
+#define DSA_GEMM_LAUNCH(BN_, OB_) \
+    gemm_tc_kernel<BN_, OB_><<<grid, kGemmThreads, GemmTc<BN_>::SMEM, st>>>(ta, tb, m, n, k, c, ldc, to)
+    if (out_bf16) {
+        if (bn == 256) DSA_GEMM_LAUNCH(256, true); else if (bn == 128) DSA_GEMM_LAUNCH(128, true); else DSA_GEMM_LAUNCH(64, true);
+    } else {
+        if (bn == 256) DSA_GEMM_LAUNCH(256, false); else if (bn == 128) DSA_GEMM_LAUNCH(128, false); else DSA_GEMM_LAUNCH(64, false);
+    }
+#undef DSA_GEMM_LAUNCH
+    return launch_status();
+}
+
 int run_index_scores(const dsa_params* p, const void* q_idx, const float* w, const void* k_idx, const RowSpec& rs,
                      int rows, long long key_rows, float* scores, long long ld, cudaStream_t st) {
     DevInfo* di = nullptr;
@@ -655,4 +699,59 @@ extern "C" int dsa_forward_decode_noalloc(const dsa_params* params, const void* 
     if ((rc = run_index_scores(params, q_idx, w, idx_cache, rs, batch, key_rows, scores, ld, st)) != DSA_OK) return rc;
     if ((rc = run_topk(params, scores, ld, rs, batch, idx, st)) != DSA_OK) return rc;
     return run_attn(params, q, kv_cache, idx, rs, batch, key_rows, out, lse, st);
+}
+
+// ---------------------------------------------------------------------------
+// upstream of the path: the indexer's input projections and its cache update
+// ---------------------------------------------------------------------------
+extern "C" int dsa_gemm_bf16(const void* a, long long lda, const void* b, long long ldb, int m, int n, int k, void* c,
+                             long long ldc, int c_dtype, void* stream) {
+    if (a == nullptr || b == nullptr || c == nullptr) return DSA_ERR_ARG;
+    if (m < 1 || n < 1 || k < 1 || (c_dtype != DSA_BF16 && c_dtype != DSA_FP32)) return DSA_ERR_ARG;
+    if (lda < k || ldb < k || ldc < n) return DSA_ERR_SHAPE;
+    // TMA: 16-byte aligned bases and row strides; the epilogue's 16-byte stores likewise
+    if (!aligned16(a) || !aligned16(b) || !aligned16(c) || lda % 8 != 0 || ldb % 8 != 0 ||
+        ldc % (c_dtype == DSA_BF16 ? 8 : 4) != 0)
+        return DSA_ERR_SHAPE;
+    if (m > 65535 * kGemmBM) return DSA_ERR_UNSUPPORTED;
+    return run_gemm(a, lda, b, ldb, m, n, k, c, ldc, c_dtype == DSA_BF16, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int dsa_indexer_inputs(const dsa_params* params, const void* q_latent, const void* x, const void* wq_b,
+                                  const void* wk, const void* w_proj, int total_q, int q_lora_rank, int hidden,
+                                  void* q_idx, void* k_idx, float* w, void* stream) {
+    int rc = check_params(params);
+    if (rc != DSA_OK) return rc;
+    if (params->dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
+    if (total_q < 0 || q_lora_rank < 1 || hidden < 1) return DSA_ERR_ARG;
+    if (total_q == 0) return DSA_OK;
+    if (q_latent == nullptr || x == nullptr || wq_b == nullptr || wk == nullptr || w_proj == nullptr ||
+        q_idx == nullptr || k_idx == nullptr || w == nullptr)
+        return DSA_ERR_ARG;
+    const int H = params->n_idx_heads, D = params->idx_dim;
+    if (q_lora_rank % 8 != 0 || hidden % 8 != 0 || (H * D) % 8 != 0 || D % 8 != 0 || H % 4 != 0) return DSA_ERR_SHAPE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((rc = dsa_gemm_bf16(q_latent, q_lora_rank, wq_b, q_lora_rank, total_q, H * D, q_lora_rank, q_idx, H * D,
+                            DSA_BF16, st)) != DSA_OK)
+        return rc;
+    if ((rc = dsa_gemm_bf16(x, hidden, wk, hidden, total_q, D, hidden, k_idx, D, DSA_BF16, st)) != DSA_OK) return rc;
+    return dsa_gemm_bf16(x, hidden, w_proj, hidden, total_q, H, hidden, w, H, DSA_FP32, st);
+}
+
+extern "C" int dsa_update_indexer(const dsa_params* params, const void* k_new, const void* kv_new, int batch,
+                                  int max_ctx, int* cache_seqlens, void* idx_cache, void* kv_cache, void* stream) {
+    int rc = check_params(params);
+    if (rc != DSA_OK) return rc;
+    if (batch < 1 || max_ctx < 1) return DSA_ERR_ARG;
+    if (k_new == nullptr || kv_new == nullptr || cache_seqlens == nullptr || idx_cache == nullptr ||
+        kv_cache == nullptr)
+        return DSA_ERR_ARG;
+    const int es = params->dtype == DSA_BF16 ? 2 : 4;
+    const int kb = params->idx_dim * es, vb = params->d_qk * es;
+    if (kb % 16 != 0 || vb % 16 != 0) return DSA_ERR_SHAPE;
+    if (!aligned16(k_new) || !aligned16(kv_new) || !aligned16(idx_cache) || !aligned16(kv_cache)) return DSA_ERR_ARG;
+    update_indexer_kernel<<<batch, kUpdThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(kv_new), batch, max_ctx, kb, vb, cache_seqlens,
+        static_cast<uint8_t*>(idx_cache), static_cast<uint8_t*>(kv_cache));
+    return launch_status();
 }

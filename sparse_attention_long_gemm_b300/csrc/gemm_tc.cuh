@@ -1,0 +1,211 @@
+// gemm_tc.cuh -- the Lightning Indexer's input projections on the sm_103a
+// tensor cores, and the decode step's key-cache append.
+//
+// DeepSeek-V3.2 page, "DeepSeek Sparse Attention (DSA)": the indexer scores
+// queries taken from the MLA query latent through its projection wq_b (sized
+// by q_lora_rank), weights its heads with the weights_proj module, and keeps
+// its own single-head key cache of index_head_dim per token, updated through
+// update_indexer().  The projections are bias-free linear maps,
+//     C[M, N] = A[M, K] . B[N, K]^T
+// with A the activations (tokens x K) and B the weight (N outputs x K), both
+// bf16 with K contiguous; the products accumulate in fp32 in tensor memory and
+// C is written as bf16 (indexer queries and keys) or fp32 (head weights).
+//
+// gemm_tc_kernel: one 128 x BN tile of C per CTA (128 threads).
+//   - one thread streams 128 x 64 tiles of A and BN x 64 tiles of B by TMA
+//     (128-byte swizzle) through a 4-stage ring;
+//   - one thread issues tcgen05.mma kind::f16 (M = 128, N = BN, K = 16, four
+//     per 64-wide K step) into a BN-column fp32 accumulator in tensor memory
+//     and frees each stage with tcgen05.commit;
+//   - all four warps then read their 32 accumulator lanes (rows) back with
+//     tcgen05.ld and store them, converted, with 16-byte stores.
+// Rows past M and columns past N are zero-filled by TMA on load and masked on
+// store; a K that is not a multiple of 64 reads zeros past its end.
+//
+// update_indexer_kernel: one CTA per sequence copies the new token's indexer
+// key and latent row to position cache_seqlens[b] of its caches and advances
+// the length.  A length outside [0, max_ctx) (no room) writes nothing and
+// raises DSA_ERR_DEVICE_DATA.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace dsa {
+
+constexpr int kGemmBM = 128;
+constexpr int kGemmBK = 64;
+constexpr int kGemmStages = 4;
+constexpr int kGemmThreads = 128;
+
+template <int BN>
+struct GemmTc {
+    static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+    static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;      // 16 KB
+    static constexpr int B_BYTES = BN * kGemmBK * 2;           // 8 .. 32 KB
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int OFF_BAR = kGemmStages * STAGE;
+    static constexpr int NBAR = 2 * kGemmStages + 1;           // full[S], empty[S], acc_full
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_MISC + 16 + 1024;          // + alignment slack
+    static constexpr uint32_t IDESC = idesc_bf16(kGemmBM, BN, false, false);
+    static constexpr int TMEM_COLS = BN;
+};
+static_assert(GemmTc<256>::SMEM <= 232448, "gemm shared memory exceeds the per-CTA limit");
+static_assert(GemmTc<64>::STAGE % 1024 == 0 && GemmTc<128>::STAGE % 1024 == 0 && GemmTc<256>::STAGE % 1024 == 0,
+              "stages hold 128B-swizzled tiles (1024-byte atoms)");
+
+template <int BN, bool OUT_BF16>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, int M, int N,
+               int K, void* __restrict__ c, long long ldc, unsigned long long timeout_ns) {
+    using G = GemmTc<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + G::OFF_BAR;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (kGemmStages + s); };
+    const uint32_t acc_full = bar0 + 8u * (2 * kGemmStages);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::OFF_MISC);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + G::OFF_MISC + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kGemmBM;
+    const int nk = (K + kGemmBK - 1) / kGemmBK;
+
+    if (tid == 0) {
+        for (int s = 0; s < kGemmStages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+        mbar_init(acc_full, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), G::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % kGemmStages;
+            if (!wait_bar(empty(s), ((kb / kGemmStages) & 1) ^ 1, timeout_ns, s_abort)) break;
+            const uint32_t st = sbase + static_cast<uint32_t>(s * G::STAGE);
+            mbar_expect_tx(full(s), G::STAGE);
+            tma_load_2d(st, &tm_a, kb * kGemmBK, m0, full(s));
+            tma_load_2d(st + G::A_BYTES, &tm_b, kb * kGemmBK, n0, full(s));
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        bool ok = true;
+        for (int kb = 0; kb < nk && ok; ++kb) {
+            const int s = kb % kGemmStages;
+            ok = wait_bar(full(s), (kb / kGemmStages) & 1, timeout_ns, s_abort);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t st = sbase + static_cast<uint32_t>(s * G::STAGE);
+            const uint64_t da = sdesc_sw128(st, 16, 1024), db = sdesc_sw128(st + G::A_BYTES, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kGemmBK / 16; ++kk)
+                tc_mma_bf16(tmem, da + static_cast<uint64_t>((kk * 32) >> 4), db + static_cast<uint64_t>((kk * 32) >> 4),
+                            G::IDESC, (kb | kk) ? 1u : 0u);
+            tc_commit(empty(s));
+        }
+        tc_commit(acc_full);   // also on the abort path: the epilogue's wait then ends at once
+    }
+    __syncwarp();
+
+    // ---------------- epilogue: warp w reads accumulator lanes (rows) 32w .. 32w+31 ----------------
+    const bool acc_ok = wait_bar(acc_full, 0, timeout_ns, s_abort) && *s_abort == 0;
+    if (__all_sync(0xffffffffu, acc_ok)) {
+        tc_fence_after();
+        const int row = m0 + warp * 32 + lane;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(taddr + static_cast<uint32_t>(c0), v);
+            tmem_ld_wait();
+            const int col = n0 + c0;
+            if (row >= M || col >= N) continue;
+            const bool whole = col + 32 <= N;
+            if constexpr (OUT_BF16) {
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(c) + static_cast<long long>(row) * ldc + col;
+                if (whole) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]),
+                                                                           __uint_as_float(v[8 * q + 2 * e + 1]));
+                            pk[e] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
+                        reinterpret_cast<uint4*>(dst)[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < N - col) dst[j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                }
+            } else {
+                float* dst = static_cast<float*>(c) + static_cast<long long>(row) * ldc + col;
+                if (whole) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        reinterpret_cast<float4*>(dst)[q] =
+                            make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                        __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < N - col) dst[j] = __uint_as_float(v[j]);
+                }
+            }
+        }
+    }
+    if (*s_abort) sleep_ns(1000000ull);   // loads already issued land before the CTA exits
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, G::TMEM_COLS);
+    }
+}
+
+constexpr int kUpdThreads = 128;
+
+// One CTA per sequence: the new token's indexer key (k_bytes per sequence) and latent row
+// (kv_bytes) go to position cache_seqlens[b] of idx_cache [batch, max_ctx, k_bytes] and
+// kv_cache [batch, max_ctx, kv_bytes], and the length grows by one.  Row sizes are multiples
+// of 16 bytes and the arrays 16-byte aligned.
+__global__ void __launch_bounds__(kUpdThreads)
+update_indexer_kernel(const uint8_t* __restrict__ k_new, const uint8_t* __restrict__ kv_new, int batch, int max_ctx,
+                      int k_bytes, int kv_bytes, int* __restrict__ cache_seqlens, uint8_t* __restrict__ idx_cache,
+                      uint8_t* __restrict__ kv_cache) {
+    const int b = blockIdx.x;
+    if (b >= batch) return;
+    const int p = cache_seqlens[b];
+    if (p < 0 || p >= max_ctx) {   // no room (or a corrupt length): nothing is written
+        if (threadIdx.x == 0) raise_error(DSA_ERR_DEVICE_DATA);
+        return;
+    }
+    const long long slot = static_cast<long long>(b) * max_ctx + p;
+    const uint4* ks = reinterpret_cast<const uint4*>(k_new + static_cast<long long>(b) * k_bytes);
+    uint4* kd = reinterpret_cast<uint4*>(idx_cache + slot * k_bytes);
+    for (int i = threadIdx.x; i < k_bytes / 16; i += kUpdThreads) kd[i] = ks[i];
+    const uint4* vs = reinterpret_cast<const uint4*>(kv_new + static_cast<long long>(b) * kv_bytes);
+    uint4* vd = reinterpret_cast<uint4*>(kv_cache + slot * kv_bytes);
+    for (int i = threadIdx.x; i < kv_bytes / 16; i += kUpdThreads) vd[i] = vs[i];
+    __syncthreads();   // every thread has read the length before it changes
+    if (threadIdx.x == 0) cache_seqlens[b] = p + 1;
+}
+
+}  // namespace dsa

@@ -134,3 +134,28 @@ def test_fp8_indexer_flag_is_checked_on_the_host(L):
     assert extra == T * 64 * 128 + 25600 + 12800 + 512   # q8, w*s_q, k8, s_k, each 256-aligned
     tiny = B.make_params(**TINY)
     assert L.dsa_indexer_quantize_fp8(ctypes.byref(tiny), f, 4, None, f, f, None) == B.DSA_ERR_UNSUPPORTED
+
+
+def test_indexer_inputs_and_update_are_checked_on_the_host(L):
+    f = ctypes.c_void_p(0x10000)          # 16-byte aligned, never dereferenced: every case fails first
+    g = ctypes.c_void_p(0x10008)          # 8-byte aligned only
+    ok = (f, 64, f, 64, 128, 256, 64, f, 256, B.DSA_BF16, None)
+    assert L.dsa_gemm_bf16(None, *ok[1:]) == B.DSA_ERR_ARG
+    assert L.dsa_gemm_bf16(*ok[:4], 0, *ok[5:]) == B.DSA_ERR_ARG                       # m < 1
+    assert L.dsa_gemm_bf16(*ok[:9], 7, None) == B.DSA_ERR_ARG                          # bad c_dtype
+    assert L.dsa_gemm_bf16(f, 60, *ok[2:]) == B.DSA_ERR_SHAPE                          # lda < k
+    assert L.dsa_gemm_bf16(f, 68, *ok[2:]) == B.DSA_ERR_SHAPE                          # lda not a multiple of 8
+    assert L.dsa_gemm_bf16(g, *ok[1:]) == B.DSA_ERR_SHAPE                              # misaligned A
+    assert L.dsa_gemm_bf16(*ok[:8], 260, B.DSA_BF16, None) == B.DSA_ERR_SHAPE          # bf16 ldc % 8
+    assert L.dsa_gemm_bf16(*ok[:4], 65535 * 128 + 1, *ok[5:]) == B.DSA_ERR_UNSUPPORTED
+    p = B.make_params(**V32)
+    tiny = B.make_params(**TINY)
+    args = (f, f, f, f, f, 100, 1536, 7168, f, f, f, None)
+    assert L.dsa_indexer_inputs(ctypes.byref(tiny), *args) == B.DSA_ERR_UNSUPPORTED    # fp32 params
+    assert L.dsa_indexer_inputs(ctypes.byref(p), *args[:5], 100, 1530, 7168, *args[8:]) == B.DSA_ERR_SHAPE
+    assert L.dsa_indexer_inputs(ctypes.byref(p), *args[:5], -1, *args[6:]) == B.DSA_ERR_ARG
+    assert L.dsa_indexer_inputs(ctypes.byref(p), *args[:5], 0, *args[6:]) == B.DSA_OK     # nothing to do
+    assert L.dsa_indexer_inputs(ctypes.byref(p), None, *args[1:]) == B.DSA_ERR_ARG
+    assert L.dsa_update_indexer(ctypes.byref(p), f, f, 0, 64, f, f, f, None) == B.DSA_ERR_ARG
+    assert L.dsa_update_indexer(ctypes.byref(p), f, None, 2, 64, f, f, f, None) == B.DSA_ERR_ARG
+    assert L.dsa_update_indexer(ctypes.byref(p), g, f, 2, 64, f, f, f, None) == B.DSA_ERR_ARG
