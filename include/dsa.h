@@ -259,6 +259,29 @@ int dsa_index_scores_fp8_decode(const dsa_params* params, const void* q8, const 
  *   device error word.  Rows must be multiples of 16 bytes and the arrays
  *   16-byte aligned (DSA_ERR_SHAPE / DSA_ERR_ARG otherwise).  The caches are
  *   the dense layout the decode calls read. */
+/* Paged ("dynamic") caches.  The indexer key cache and the latent cache are
+ * pools of num_pages pages of page_size positions (idx_pool [num_pages *
+ * page_size, D_I], kv_pool [num_pages * page_size, d_qk]); position s of
+ * sequence b sits in page block_table[b * max_pages + s / page_size] (device
+ * int32 [batch, max_pages]) at offset s % page_size.  page_size is a power of
+ * two in [128, 2^20] (a 128-key indexer tile never crosses a page), num_pages *
+ * page_size <= 2^31 - 1, max_pages * page_size <= 2^20.  A page index outside
+ * [0, num_pages) is read as page 0 and raises DSA_ERR_DEVICE_DATA.
+ * dsa_forward_decode_paged: dsa_forward_decode over paged caches, with
+ *   max_ctx = max_pages * page_size (the score rows, the workspace size of
+ *   dsa_decode_workspace_size(params, batch, max_ctx) and the selected
+ *   positions are in that logical position space).  Same results as
+ *   dsa_forward_decode over the dense caches the pages stand for.
+ * dsa_update_indexer_paged: dsa_update_indexer into paged caches. */
+int dsa_forward_decode_paged(const dsa_params* params, const void* q_idx, const float* w,
+                             const void* q, const void* idx_pool, const void* kv_pool,
+                             int num_pages, int page_size, const int* block_table, int max_pages,
+                             const int* cache_seqlens, int batch, void* out, float* lse,
+                             int* idx_out, void* workspace, size_t workspace_bytes, void* stream);
+int dsa_update_indexer_paged(const dsa_params* params, const void* k_new, const void* kv_new,
+                             int batch, int* cache_seqlens, void* idx_pool, void* kv_pool,
+                             int num_pages, int page_size, const int* block_table, int max_pages,
+                             void* stream);
 int dsa_gemm_bf16(const void* a, long long lda, const void* b, long long ldb, int m, int n, int k,
                   void* c, long long ldc, int c_dtype, void* stream);
 int dsa_indexer_inputs(const dsa_params* params, const void* q_latent, const void* x,

@@ -12,6 +12,7 @@ from .dsa_oracle import (  # noqa: F401
     indexer_inputs,
     linear,
     masked_attention_row,
+    paged_to_dense,
     topk_select,
     update_indexer,
 )

@@ -421,3 +421,21 @@ def update_indexer(idx_cache, kv_cache, cache_seqlens, k_new, kv_new):
         kv[b, p] = kv_new[b]
         lens[b] = p + 1
     return idx, kv, lens, full
+
+
+def paged_to_dense(pool, block_table, page_size):
+    """A paged cache as the dense cache it stands for: the pool [num_pages * page_size, d] holds
+    pages of page_size positions, and position s of sequence b sits in page
+    block_table[b, s // page_size] at offset s % page_size ("DeepSeek-V3.2" page: the cache
+    layers are dynamic or static; a block table is the plainest form of a dynamic one).
+    Returns [B, max_pages * page_size, d]; positions of table entries < 0 are zero."""
+    pool = np.asarray(pool)
+    table = np.asarray(block_table)
+    B, P = table.shape
+    out = np.zeros((B, P * page_size) + pool.shape[1:], dtype=pool.dtype)
+    for b in range(B):
+        for j in range(P):
+            pg = int(table[b, j])
+            if pg >= 0:
+                out[b, j * page_size:(j + 1) * page_size] = pool[pg * page_size:(pg + 1) * page_size]
+    return out

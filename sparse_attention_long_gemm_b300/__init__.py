@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     dsa_decode_workspace_size,
     dsa_forward,
     dsa_forward_decode,
+    dsa_forward_decode_paged,
     dsa_gemm_bf16,
     dsa_get_device_error,
     dsa_index_scores,
@@ -37,6 +38,7 @@ from ._binding import (  # noqa: F401
     dsa_topk,
     dsa_topk_decode,
     dsa_update_indexer,
+    dsa_update_indexer_paged,
     dsa_workspace_size,
     make_params,
     params_from_config,

@@ -49,6 +49,8 @@ EXPORTED = [
     "dsa_gemm_bf16",
     "dsa_indexer_inputs",
     "dsa_update_indexer",
+    "dsa_forward_decode_paged",
+    "dsa_update_indexer_paged",
 ]
 
 
@@ -122,6 +124,10 @@ def lib():
         L.dsa_gemm_bf16.argtypes = [vp, ll, vp, ll, i, i, i, vp, ll, i, vp]
         L.dsa_indexer_inputs.restype = i
         L.dsa_indexer_inputs.argtypes = [P, vp, vp, vp, vp, vp, i, i, i, vp, vp, vp, vp]
+        L.dsa_forward_decode_paged.restype = i
+        L.dsa_forward_decode_paged.argtypes = [P, vp, vp, vp, vp, vp, i, i, vp, i, vp, i, vp, vp, vp, vp, sz, vp]
+        L.dsa_update_indexer_paged.restype = i
+        L.dsa_update_indexer_paged.argtypes = [P, vp, vp, i, vp, vp, vp, i, i, vp, i, vp]
         L.dsa_update_indexer.restype = i
         L.dsa_update_indexer.argtypes = [P, vp, vp, i, i, vp, vp, vp, vp]
         L.dsa_get_device_error.restype = i
@@ -277,6 +283,23 @@ def dsa_update_indexer(p, k_new, kv_new, batch, max_ctx, cache_seqlens, idx_cach
     rc = lib().dsa_update_indexer(ctypes.byref(p), _ptr(k_new), _ptr(kv_new), batch, max_ctx, _ptr(cache_seqlens),
                                   _ptr(idx_cache), _ptr(kv_cache), _stream(stream))
     _check(rc, "dsa_update_indexer")
+
+
+def dsa_forward_decode_paged(p, q_idx, w, q, idx_pool, kv_pool, num_pages, page_size, block_table, max_pages,
+                             cache_seqlens, batch, out, lse, idx_out, workspace, workspace_bytes, stream=None):
+    rc = lib().dsa_forward_decode_paged(ctypes.byref(p), _ptr(q_idx), _ptr(w), _ptr(q), _ptr(idx_pool), _ptr(kv_pool),
+                                        num_pages, page_size, _ptr(block_table), max_pages, _ptr(cache_seqlens), batch,
+                                        _ptr(out), _ptr(lse), _ptr(idx_out), _ptr(workspace), workspace_bytes,
+                                        _stream(stream))
+    _check(rc, "dsa_forward_decode_paged")
+
+
+def dsa_update_indexer_paged(p, k_new, kv_new, batch, cache_seqlens, idx_pool, kv_pool, num_pages, page_size,
+                             block_table, max_pages, stream=None):
+    rc = lib().dsa_update_indexer_paged(ctypes.byref(p), _ptr(k_new), _ptr(kv_new), batch, _ptr(cache_seqlens),
+                                        _ptr(idx_pool), _ptr(kv_pool), num_pages, page_size, _ptr(block_table),
+                                        max_pages, _stream(stream))
+    _check(rc, "dsa_update_indexer_paged")
 
 
 def dsa_get_device_error(stream=None) -> int:

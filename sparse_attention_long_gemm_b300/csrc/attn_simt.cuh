@@ -48,7 +48,7 @@ attn_simt_kernel(RowSpec rs, const T* __restrict__ q, const T* __restrict__ kv, 
     for (int i = tid; i < k; i += kAttnSimtThreads) {
         float z = -INFINITY;
         if (sidx[i] >= 0) {
-            const T* kr = kv + (ri.key_base + sidx[i]) * d_qk;
+            const T* kr = kv + key_row(rs, r, ri.key_base, sidx[i]) * d_qk;
             float dot = 0.f;
             for (int d = 0; d < d_qk; ++d) dot = fmaf(sq[d], to_f32(kr[d]), dot);
             z = dot * scale;
@@ -87,7 +87,7 @@ attn_simt_kernel(RowSpec rs, const T* __restrict__ q, const T* __restrict__ kv, 
         float o = 0.f;
         for (int i = 0; i < k; ++i) {
             const int s = sidx[i];
-            if (s >= 0) o = fmaf(sz[i], to_f32(kv[(ri.key_base + s) * d_qk + c]), o);
+            if (s >= 0) o = fmaf(sz[i], to_f32(kv[key_row(rs, r, ri.key_base, s) * d_qk + c]), o);
         }
         orow[c] = from_f32<T>(o * inv);
     }

@@ -210,6 +210,8 @@ __device__ __forceinline__ AttnRow attn_row(const RowSpec& rs, int r, int k) {
     return a;
 }
 
+// PAGED: the selected rows come from paged pools through the block table of `rs`.
+template <bool PAGED = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_q_rope,
                const __nv_bfloat16* __restrict__ kv, const int* __restrict__ idx, RowSpec rs, int rows, int k,
@@ -329,7 +331,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     if (i * kAttnBK + pw * 32 + lane < A.nsel) raise_error(DSA_ERR_DEVICE_DATA);
                     s_ = 0;   // any in-range row; entries past nsel are masked by the softmax
                 }
-                const long long myrow = kb + s_;
+                const long long myrow = PAGED ? key_row_paged(rs, r, s_) : kb + s_;
                 e0 = e1; e1 = e2; e2 = e3;
                 e3 = ld_ent(i + 4);
                 ok = wait_bar(empty(rp % kAttnSlots), ((rp / kAttnSlots) & 1) ^ 1, timeout_ns, s_abort);

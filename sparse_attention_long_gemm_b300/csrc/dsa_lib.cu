@@ -96,7 +96,10 @@ int device_info(DevInfo** out) {
             IdxTc<kPreNQ, kF8PreKS, kPreQB, true>::SMEM);
         set(reinterpret_cast<const void*>(&indexer_tc_kernel<kDecNQ, kF8DecKS, kDecQB, true>),
             IdxTc<kDecNQ, kF8DecKS, kDecQB, true>::SMEM);
-        set(reinterpret_cast<const void*>(&attn_tc_kernel), AttnTc::SMEM);
+        set(reinterpret_cast<const void*>(&attn_tc_kernel<false>), AttnTc::SMEM);
+        set(reinterpret_cast<const void*>(&attn_tc_kernel<true>), AttnTc::SMEM);
+        set(reinterpret_cast<const void*>(&indexer_tc_kernel<kDecNQ, kDecKS, kDecQB, false, true>),
+            IdxTc<kDecNQ, kDecKS, kDecQB>::SMEM);
         set(reinterpret_cast<const void*>(&gemm_tc_kernel<64, true>), GemmTc<64>::SMEM);
         set(reinterpret_cast<const void*>(&gemm_tc_kernel<128, true>), GemmTc<128>::SMEM);
         set(reinterpret_cast<const void*>(&gemm_tc_kernel<256, true>), GemmTc<256>::SMEM);
@@ -228,8 +231,12 @@ int run_index_scores(const dsa_params* p, const void* q_idx, const float* w, con
                     <<<di->sm_count, C::THREADS, C::SMEM, st>>>(tq, tk, ch, w, nullptr, scores, ld, kPreKC, to);
             } else {
                 using C = IdxTc<kDecNQ, kDecKS, kDecQB>;
-                indexer_tc_kernel<kDecNQ, kDecKS, kDecQB>
-                    <<<di->sm_count, C::THREADS, C::SMEM, st>>>(tq, tk, ch, w, nullptr, scores, ld, kDecKC, to);
+                if (rs.pages != nullptr)
+                    indexer_tc_kernel<kDecNQ, kDecKS, kDecQB, false, true>
+                        <<<di->sm_count, C::THREADS, C::SMEM, st>>>(tq, tk, ch, w, nullptr, scores, ld, kDecKC, to);
+                else
+                    indexer_tc_kernel<kDecNQ, kDecKS, kDecQB>
+                        <<<di->sm_count, C::THREADS, C::SMEM, st>>>(tq, tk, ch, w, nullptr, scores, ld, kDecKC, to);
             }
             if ((rc = launch_status()) != DSA_OK) return rc;
         }
@@ -329,9 +336,15 @@ int run_attn(const dsa_params* p, const void* q, const void* kv, const int* idx,
         (void)key_rows;
         const float scale_log2 = p->softmax_scale * 1.4426950408889634f;
         const int nclusters = std::max(1, std::min(rows, di->sm_count / 2));
-        attn_tc_kernel<<<2 * nclusters, kAttnThreads, AttnTc::SMEM, st>>>(
-            tq, tqr, static_cast<const __nv_bfloat16*>(kv), idx, rs, rows, p->topk, scale_log2,
-            static_cast<__nv_bfloat16*>(out), lse, static_cast<unsigned long long>(g_timeout_ns.load()));
+        const unsigned long long to = static_cast<unsigned long long>(g_timeout_ns.load());
+        if (rs.pages != nullptr)
+            attn_tc_kernel<true><<<2 * nclusters, kAttnThreads, AttnTc::SMEM, st>>>(
+                tq, tqr, static_cast<const __nv_bfloat16*>(kv), idx, rs, rows, p->topk, scale_log2,
+                static_cast<__nv_bfloat16*>(out), lse, to);
+        else
+            attn_tc_kernel<false><<<2 * nclusters, kAttnThreads, AttnTc::SMEM, st>>>(
+                tq, tqr, static_cast<const __nv_bfloat16*>(kv), idx, rs, rows, p->topk, scale_log2,
+                static_cast<__nv_bfloat16*>(out), lse, to);
         return launch_status();
     }
     const dim3 grid(rows, p->n_heads);
@@ -738,11 +751,24 @@ extern "C" int dsa_indexer_inputs(const dsa_params* params, const void* q_latent
     return dsa_gemm_bf16(x, hidden, w_proj, hidden, total_q, H, hidden, w, H, DSA_FP32, st);
 }
 
-extern "C" int dsa_update_indexer(const dsa_params* params, const void* k_new, const void* kv_new, int batch,
-                                  int max_ctx, int* cache_seqlens, void* idx_cache, void* kv_cache, void* stream) {
-    int rc = check_params(params);
-    if (rc != DSA_OK) return rc;
-    if (batch < 1 || max_ctx < 1) return DSA_ERR_ARG;
+namespace {
+// Validates a paged cache (page pools of num_pages pages of page_size positions, block table
+// [batch, max_pages]) and fills the paged fields of rs.
+int paged_spec(int num_pages, int page_size, const int* block_table, int max_pages, RowSpec* rs) {
+    if (block_table == nullptr || num_pages < 1 || max_pages < 1) return DSA_ERR_ARG;
+    if (page_size < 128 || page_size > (1 << 20) || (page_size & (page_size - 1)) != 0) return DSA_ERR_SHAPE;
+    if (static_cast<long long>(num_pages) * page_size > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+    int lg = 0;
+    while ((1 << lg) < page_size) ++lg;
+    rs->pages = block_table;
+    rs->page_log2 = lg;
+    rs->max_pages = max_pages;
+    rs->num_pages = num_pages;
+    return DSA_OK;
+}
+
+int update_indexer(const dsa_params* params, const void* k_new, const void* kv_new, const RowSpec& rs,
+                   int* cache_seqlens, void* idx_cache, void* kv_cache, void* stream) {
     if (k_new == nullptr || kv_new == nullptr || cache_seqlens == nullptr || idx_cache == nullptr ||
         kv_cache == nullptr)
         return DSA_ERR_ARG;
@@ -750,8 +776,66 @@ extern "C" int dsa_update_indexer(const dsa_params* params, const void* k_new, c
     const int kb = params->idx_dim * es, vb = params->d_qk * es;
     if (kb % 16 != 0 || vb % 16 != 0) return DSA_ERR_SHAPE;
     if (!aligned16(k_new) || !aligned16(kv_new) || !aligned16(idx_cache) || !aligned16(kv_cache)) return DSA_ERR_ARG;
-    update_indexer_kernel<<<batch, kUpdThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(kv_new), batch, max_ctx, kb, vb, cache_seqlens,
+    update_indexer_kernel<<<rs.batch, kUpdThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        rs, static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(kv_new), kb, vb, cache_seqlens,
         static_cast<uint8_t*>(idx_cache), static_cast<uint8_t*>(kv_cache));
     return launch_status();
+}
+}  // namespace
+
+extern "C" int dsa_update_indexer(const dsa_params* params, const void* k_new, const void* kv_new, int batch,
+                                  int max_ctx, int* cache_seqlens, void* idx_cache, void* kv_cache, void* stream) {
+    int rc = check_params(params);
+    if (rc != DSA_OK) return rc;
+    if (batch < 1 || max_ctx < 1) return DSA_ERR_ARG;
+    const RowSpec rs{cache_seqlens, batch, 1, max_ctx};
+    return update_indexer(params, k_new, kv_new, rs, cache_seqlens, idx_cache, kv_cache, stream);
+}
+
+extern "C" int dsa_update_indexer_paged(const dsa_params* params, const void* k_new, const void* kv_new, int batch,
+                                        int* cache_seqlens, void* idx_pool, void* kv_pool, int num_pages,
+                                        int page_size, const int* block_table, int max_pages, void* stream) {
+    int rc = check_params(params);
+    if (rc != DSA_OK) return rc;
+    if (batch < 1) return DSA_ERR_ARG;
+    RowSpec rs{cache_seqlens, batch, 1, 0};
+    if ((rc = paged_spec(num_pages, page_size, block_table, max_pages, &rs)) != DSA_OK) return rc;
+    if (static_cast<long long>(max_pages) * page_size > (1 << 20)) return DSA_ERR_UNSUPPORTED;
+    rs.max_len = max_pages * page_size;
+    return update_indexer(params, k_new, kv_new, rs, cache_seqlens, idx_pool, kv_pool, stream);
+}
+
+extern "C" int dsa_forward_decode_paged(const dsa_params* params, const void* q_idx, const float* w, const void* q,
+                                        const void* idx_pool, const void* kv_pool, int num_pages, int page_size,
+                                        const int* block_table, int max_pages, const int* cache_seqlens, int batch,
+                                        void* out, float* lse, int* idx_out, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    if (params == nullptr) return DSA_ERR_ARG;
+    RowSpec rs{cache_seqlens, batch, 1, 0};
+    int rc = paged_spec(num_pages, page_size, block_table, max_pages, &rs);
+    if (rc != DSA_OK) return rc;
+    if (static_cast<long long>(max_pages) * page_size > (1 << 20)) return DSA_ERR_UNSUPPORTED;
+    const int max_ctx = max_pages * page_size;
+    rs.max_len = max_ctx;
+    if ((rc = check_decode_common(params, cache_seqlens, batch, max_ctx)) != DSA_OK) return rc;
+    if (params->indexer_fp8) return DSA_ERR_UNSUPPORTED;
+    if (q_idx == nullptr || w == nullptr || q == nullptr || idx_pool == nullptr || kv_pool == nullptr ||
+        out == nullptr)
+        return DSA_ERR_ARG;
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(q) || !aligned16(idx_pool) || !aligned16(kv_pool) ||
+        !aligned16(out) || (lse && !aligned16(lse)) || (idx_out && !aligned16(idx_out)))
+        return DSA_ERR_ARG;
+    const size_t need = dsa_decode_workspace_size(params, batch, max_ctx);
+    if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return DSA_ERR_WORKSPACE;
+    const long long ld = round_up(max_ctx, 4);
+    float* scores = static_cast<float*>(workspace);
+    int* idx = idx_out ? idx_out
+                       : reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                                round_up(static_cast<long long>(batch) * ld * 4, 256));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long key_rows = static_cast<long long>(num_pages) * page_size;
+    if ((rc = run_index_scores(params, q_idx, w, idx_pool, rs, batch, key_rows, scores, ld, st)) != DSA_OK) return rc;
+    if ((rc = run_topk(params, scores, ld, rs, batch, idx, st)) != DSA_OK) return rc;
+    return run_attn(params, q, kv_pool, idx, rs, batch, key_rows, out, lse, st);
 }

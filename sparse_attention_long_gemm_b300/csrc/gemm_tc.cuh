@@ -23,14 +23,15 @@
 // store; a K that is not a multiple of 64 reads zeros past its end.
 //
 // update_indexer_kernel: one CTA per sequence copies the new token's indexer
-// key and latent row to position cache_seqlens[b] of its caches and advances
-// the length.  A length outside [0, max_ctx) (no room) writes nothing and
+// key and latent row to position cache_seqlens[b] of its caches (dense, or
+// paged through a block table) and advances the length.  A length outside [0, max_ctx) (no room) writes nothing and
 // raises DSA_ERR_DEVICE_DATA.
 #pragma once
 
 #include <cuda.h>
 
 #include "common.cuh"
+#include "rows.cuh"
 
 namespace dsa {
 
@@ -183,21 +184,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 constexpr int kUpdThreads = 128;
 
 // One CTA per sequence: the new token's indexer key (k_bytes per sequence) and latent row
-// (kv_bytes) go to position cache_seqlens[b] of idx_cache [batch, max_ctx, k_bytes] and
-// kv_cache [batch, max_ctx, kv_bytes], and the length grows by one.  Row sizes are multiples
-// of 16 bytes and the arrays 16-byte aligned.
+// (kv_bytes) go to the row of position cache_seqlens[b] in idx_cache and kv_cache (dense
+// [batch, max_ctx, .] caches, or page pools through the block table of `rs`), and the length
+// grows by one.  Row sizes are multiples of 16 bytes and the arrays 16-byte aligned.
 __global__ void __launch_bounds__(kUpdThreads)
-update_indexer_kernel(const uint8_t* __restrict__ k_new, const uint8_t* __restrict__ kv_new, int batch, int max_ctx,
+update_indexer_kernel(RowSpec rs, const uint8_t* __restrict__ k_new, const uint8_t* __restrict__ kv_new,
                       int k_bytes, int kv_bytes, int* __restrict__ cache_seqlens, uint8_t* __restrict__ idx_cache,
                       uint8_t* __restrict__ kv_cache) {
     const int b = blockIdx.x;
-    if (b >= batch) return;
+    if (b >= rs.batch) return;
     const int p = cache_seqlens[b];
-    if (p < 0 || p >= max_ctx) {   // no room (or a corrupt length): nothing is written
+    if (p < 0 || p >= rs.max_len) {   // no room (or a corrupt length): nothing is written
         if (threadIdx.x == 0) raise_error(DSA_ERR_DEVICE_DATA);
         return;
     }
-    const long long slot = static_cast<long long>(b) * max_ctx + p;
+    const long long slot = key_row(rs, b, static_cast<long long>(b) * rs.max_len, p);
     const uint4* ks = reinterpret_cast<const uint4*>(k_new + static_cast<long long>(b) * k_bytes);
     uint4* kd = reinterpret_cast<uint4*>(idx_cache + slot * k_bytes);
     for (int i = threadIdx.x; i < k_bytes / 16; i += kUpdThreads) kd[i] = ks[i];

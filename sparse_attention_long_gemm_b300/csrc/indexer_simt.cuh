@@ -46,7 +46,7 @@ indexer_simt_kernel(RowSpec rs, const T* __restrict__ q_idx, const float* __rest
         for (int i = tid; i < kIdxSimtKeys * D_I; i += kIdxSimtThreads) {
             const int kk = i / D_I, d = i - kk * D_I;
             const int s = s0 + kk;
-            sk[kk * (D_I + 1) + d] = (s < n) ? to_f32(k_idx[(ri.key_base + s) * D_I + d]) : 0.f;
+            sk[kk * (D_I + 1) + d] = (s < n) ? to_f32(k_idx[key_row(rs, r, ri.key_base, s) * D_I + d]) : 0.f;
         }
         __syncthreads();
         float acc = 0.f;

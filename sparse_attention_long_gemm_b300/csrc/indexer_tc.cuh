@@ -160,7 +160,7 @@ struct IdxSched {
 // F8: q / k are E4M3 codes of the rotated vectors, w holds w * s_q (the query scales folded
 // in) and ksc the key scales s_k, applied per key after the head sum (both scales are positive,
 // so they commute with the ReLU).
-template <int NQ, int KSTAGES, int QBUF, bool F8 = false>
+template <int NQ, int KSTAGES, int QBUF, bool F8 = false, bool PAGED = false>
 __global__ void __launch_bounds__(IdxTc<NQ, KSTAGES, QBUF, F8>::THREADS, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, RowSpec rs,
                   const float* __restrict__ w, const float* __restrict__ ksc, float* __restrict__ scores,
@@ -240,7 +240,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 ok = wait_bar(k_empty(s), ((it_k / KSTAGES) & 1) ^ 1, timeout_ns, s_abort);
                 if (!ok) break;
                 mbar_expect_tx(k_full(s), C::K_BYTES);
-                const int krow = static_cast<int>(U.key_base + static_cast<long long>(kt) * kIdxTileKeys);
+                const int krow = static_cast<int>(PAGED ? key_row_paged(rs, U.q_row0, kt * kIdxTileKeys)
+                                                        : U.key_base + static_cast<long long>(kt) * kIdxTileKeys);
                 for (int kh = 0; kh < C::KH; ++kh)
                     tma_load_2d(sK + s * C::K_BYTES + kh * C::K_HALF, &tm_k, kh * 64, krow, k_full(s));
                 ++it_k;
@@ -306,7 +307,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const int q0 = half * QPH;
                 float sk = 0.f;   // F8: this key's scale (keys past the causal range are never written)
                 if constexpr (F8) {
-                    if (s <= U.t0 + U.nq - 1) sk = __ldg(ksc + U.key_base + s);
+                    if (s <= U.t0 + U.nq - 1)
+                        sk = __ldg(ksc + (PAGED ? key_row_paged(rs, U.q_row0, s) : U.key_base + s));
                 }
                 (void)sk;
                 if (q0 < U.nq) {   // warp-uniform

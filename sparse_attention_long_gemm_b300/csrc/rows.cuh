@@ -26,6 +26,14 @@ struct RowSpec {
     int max_len;         // max_seqlen (prefill) or max_ctx (decode)
     int base;            // decode: sequence index of lens[0] (the indexer runs long batches in
                          // chunks, each with lens pointing at its first sequence); 0 otherwise
+    // decode over a paged cache: the caches are pools of num_pages pages of 2^page_log2
+    // positions, and position s of sequence b sits in page pages[b * max_pages + s >> page_log2]
+    // (page_log2 >= 7, so that a 128-key tile never crosses a page).  nullptr: dense caches,
+    // position s of sequence b at row b * max_len + s.
+    const int* pages;
+    int page_log2;
+    int max_pages;
+    int num_pages;
 };
 
 __device__ __forceinline__ RowInfo row_info(const RowSpec& rs, int r) {
@@ -47,6 +55,22 @@ __device__ __forceinline__ RowInfo row_info(const RowSpec& rs, int r) {
         raise_error(DSA_ERR_DEVICE_DATA);
     }
     return ri;
+}
+
+// Row of the key / kv pools that holds position s of decode sequence `seq` in a paged cache.
+// A page index outside the pool raises DSA_ERR_DEVICE_DATA and reads page 0 instead (an
+// in-bounds row).
+__device__ __forceinline__ long long key_row_paged(const RowSpec& rs, int seq, int s) {
+    int pg = __ldg(rs.pages + static_cast<long long>(seq) * rs.max_pages + (s >> rs.page_log2));
+    if (pg < 0 || pg >= rs.num_pages) {
+        raise_error(DSA_ERR_DEVICE_DATA);
+        pg = 0;
+    }
+    return (static_cast<long long>(pg) << rs.page_log2) + (s & ((1 << rs.page_log2) - 1));
+}
+// The same for a cache that may be dense (position s at key_base + s) or paged.
+__device__ __forceinline__ long long key_row(const RowSpec& rs, int seq, long long key_base, int s) {
+    return rs.pages == nullptr ? key_base + s : key_row_paged(rs, seq, s);
 }
 
 }  // namespace dsa

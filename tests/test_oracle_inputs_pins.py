@@ -90,3 +90,22 @@ def test_update_indexer_then_decode_sees_the_new_token():
     i2, _, l2, _ = O.update_indexer(idx, kv, lens, k_new, np.zeros((1, 3)))
     sc = O.index_scores_row(q, w, i2[0, : l2[0]])
     assert int(np.argmax(sc)) == 3 and l2[0] == 4
+
+
+def test_paged_to_dense_worked_example():
+    P = 2
+    pool = np.arange(5 * P * 3).reshape(5 * P, 3)          # 5 pages of 2 positions, 3 values each
+    table = np.array([[3, 0], [1, -1]])
+    d = O.paged_to_dense(pool, table, P)
+    assert d.shape == (2, 4, 3)
+    assert d[0, 0].tolist() == pool[6].tolist() and d[0, 1].tolist() == pool[7].tolist()   # page 3
+    assert d[0, 2].tolist() == pool[0].tolist() and d[0, 3].tolist() == pool[1].tolist()   # page 0
+    assert d[1, 0].tolist() == pool[2].tolist() and d[1, 1].tolist() == pool[3].tolist()   # page 1
+    assert np.all(d[1, 2:] == 0)                                                            # no page
+
+
+def test_paged_to_dense_with_contiguous_pages_is_a_reshape():
+    B, P, pages, D = 3, 4, 5, 2
+    pool = np.random.default_rng(0).standard_normal((B * pages * P, D))
+    table = np.arange(B * pages).reshape(B, pages)
+    assert np.array_equal(O.paged_to_dense(pool, table, P), pool.reshape(B, pages * P, D))
