@@ -687,7 +687,11 @@ def run_ours(args, cfg):
                               "frac_of_sustained": idx_tf / peak_s}),
             "topk": {"ms": stage_ms[1], "gbs": topk_gbs, "frac_of_peak": topk_gbs / peaks["hbm_gbs"]},
             "sparse_mla_attn": {"ms": stage_ms[2], "tflops": attn_tf, "frac_of_peak": attn_tf / peak_t,
-                                "frac_of_sustained": attn_tf / peak_s},
+                                "frac_of_sustained": attn_tf / peak_s,
+                                # the gather inside the kernel: every selected row's d_qk elements (split
+                                # between the two CTAs of a cluster, none fetched twice), from L2 or HBM
+                                "gather_gbs": selected * cfg.d_qk * (2 if cfg.dtype == "bf16" else 4)
+                                / (stage_ms[2] * 1e-3) / 1e9},
         },
         "roofline": {"bound": "tensor", "kernel": "attn_tc_kernel", "achieved": attn_tf, "peak": peak_t,
                      "unit": "TFLOP/s", "frac": attn_tf / peak_t, "traffic": traffic,

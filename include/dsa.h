@@ -310,7 +310,16 @@ long long dsa_set_wait_timeout_ns(long long ns);
 int dsa_selftest_wait_timeout(long long timeout_ns, void* stream);
 
 /* Name of the kernel family a call with these parameters runs:
- * "tcgen05" (sm_103a tensor-core kernels) or "simt" (general kernels). */
+ * "tcgen05" (sm_103a tensor-core kernels) or "simt" (general kernels).
+ * The tensor-core kernels take exactly the DeepSeek-V3.2 shape in bf16: 64
+ * indexer heads of 128, 128 attention heads, query/key width 576, value
+ * width 512, any index_topk, any batch and lengths.  Every other valid shape
+ * (other head counts or widths, and fp32 in any shape, such as the 4 x 32 /
+ * 8-head / 80 / 64 fp32 test configuration) runs the general CUDA-core
+ * kernels, which compute the same definitions in fp32 arithmetic.  The FP8
+ * indexer, the input projections and the paged instances of the decode
+ * kernels exist for the tensor-core shape only (the CUDA-core kernels read
+ * paged caches too).  "invalid" for parameters the library rejects. */
 const char* dsa_path_name(const dsa_params* params);
 
 /* Decode forward for callers that cannot allocate device memory.
