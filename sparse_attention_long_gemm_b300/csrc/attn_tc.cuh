@@ -44,11 +44,11 @@
 // and a small rope buffer, freeing its slots at once, so nearly the whole ring
 // holds gathers in flight: random rows reach about 9 TB/s from L2 only with
 // ~100 KB per SM in flight and with requests of 512 contiguous bytes.  The
-// rest holds the two P tiles (128B-swizzled, K-major), two buffers of received
-// partial scores (the peer sends block g + 1 while this rank still works on
-// block g, so the exchange's round trip stays off the softmax's path), a 4 KB
-// staging buffer per sending warp (16 heads per bulk copy) and the rescale
-// factors / denominators (two buffers each way).
+// rest holds the two P tiles (128B-swizzled, K-major), the received partial
+// scores (one 16 KB buffer, returned to the sender as soon as the owning warps
+// have loaded it), an 8 KB staging buffer per sending warp (its 32 heads, one
+// bulk copy per block) and the rescale factors / denominators (two buffers
+// each way).
 //
 // Per CTA (256 threads; the warp of a role depends on the rank so that the two
 // warps running the softmax have their SM sub-partitions to themselves):
@@ -57,12 +57,15 @@
 //               complete their scores, run the online softmax (running max
 //               updated lazily: O is rescaled only when it grows by more than
 //               2^8) and write their half of the P tile; the two others
-//               ("peer" warps) send their lanes' partial scores, take the
+//               ("peer" warps) send their lanes' partial scores and take the
 //               rescale factors that come with the peer's half of P
-//               (rescaling those O rows first when told to), and hand that
-//               half of the tile back to the peer once its P.V has completed.
-//               All four move Q items into tensor memory and run the output
-//               epilogue;
+//               (rescaling those O rows first when told to).  Each peer warp
+//               polls both jobs with non-blocking barrier tests, sending as
+//               soon as a block's S is in and the peer's buffer is free and
+//               taking whenever the peer's P has arrived (staging the next
+//               block's scores when neither is ready), so neither stream
+//               waits behind the other.  All four move Q items into tensor
+//               memory and run the output epilogue;
 //   one warp    copy warp (warp 4 on rank 0, warp 6 on rank 1): one thread
 //               sends this rank's half of each P tile, with its factors, to
 //               the peer by bulk copy as soon as the own warps have written
@@ -70,7 +73,9 @@
 //               wait for the peer;
 //   one warp    TMEM allocation and tcgen05.mma issue (one thread, polling
 //               both the next Q.K^T and the next P.V so neither waits on the
-//               other): warp 6 on rank 0, warp 4 on rank 1;
+//               other; after each P.V it also returns the peer's P receive
+//               buffer with a multicast tcgen05.commit): warp 6 on rank 0,
+//               warp 4 on rank 1;
 //   two warps   producers (warps 5 and 7), each gathering half of the keys of
 //               every KV item by cp.async: each warp instruction one key's 512
 //               latent bytes (the rope parts of 8 keys per instruction),
