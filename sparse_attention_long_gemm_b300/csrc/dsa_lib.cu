@@ -180,7 +180,7 @@ int make_tmap_u8(CUtensorMap* tm, const void* base, long long rows, long long co
 // ---------------------------------------------------------------------------
 // stage launchers (arguments already validated)
 // ---------------------------------------------------------------------------
-// C[M, N] = A[M, K] . B[N, K]^T: a tile width that the output columns fill
+// C[M, N] = A[M, K] . B[N, K]^T: a tile width that the output columns fill, one persistent CTA per SM
 int run_gemm(const void* a, long long lda, const void* b, long long ldb, int m, int n, int k, void* c, long long ldc,
              bool out_bf16, cudaStream_t st) {
     DevInfo* di = nullptr;
@@ -190,10 +190,19 @@ int run_gemm(const void* a, long long lda, const void* b, long long ldb, int m, 
     CUtensorMap ta, tb;
     if ((rc = make_tmap_bf16_ld(&ta, a, m, k, lda, kGemmBM)) != DSA_OK) return rc;
     if ((rc = make_tmap_bf16_ld(&tb, b, n, k, ldb, bn)) != DSA_OK) return rc;
-    const dim3 grid((n + bn - 1) / bn, (m + kGemmBM - 1) / kGemmBM);
+    const long long ntiles = static_cast<long long>((n + bn - 1) / bn) * ((m + kGemmBM - 1) / kGemmBM);
     const unsigned long long to = static_cast<unsigned long long>(g_timeout_ns.load());
-#define DSA_GEMM_LAUNCH(BN_, OB_) \
-    gemm_tc_kernel<BN_, OB_><<<grid, kGemmThreads, GemmTc<BN_>::SMEM, st>>>(ta, tb, m, n, k, c, ldc, to)
+    // persistent: as many CTAs as fit on the SMs at once (narrow tiles fit two per SM, which the
+    // bandwidth-bound projections need), at most one per tile
+#define DSA_GEMM_LAUNCH(BN_, OB_)                                                                        \
+    do {                                                                                                 \
+        int per_sm = 1;                                                                                  \
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_tc_kernel<BN_, OB_>, kGemmThreads, \
+                                                          GemmTc<BN_>::SMEM) != cudaSuccess || per_sm < 1) \
+            per_sm = 1;                                                                                  \
+        const dim3 grid(static_cast<unsigned>(std::min<long long>(ntiles, 1LL * per_sm * di->sm_count))); \
+        gemm_tc_kernel<BN_, OB_><<<grid, kGemmThreads, GemmTc<BN_>::SMEM, st>>>(ta, tb, m, n, k, c, ldc, to); \
+    } while (0)
     if (out_bf16) {
         if (bn == 256) DSA_GEMM_LAUNCH(256, true); else if (bn == 128) DSA_GEMM_LAUNCH(128, true); else DSA_GEMM_LAUNCH(64, true);
     } else {

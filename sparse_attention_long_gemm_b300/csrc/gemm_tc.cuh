@@ -11,14 +11,16 @@
 // bf16 with K contiguous; the products accumulate in fp32 in tensor memory and
 // C is written as bf16 (indexer queries and keys) or fp32 (head weights).
 //
-// gemm_tc_kernel: one 128 x BN tile of C per CTA (128 threads).
+// gemm_tc_kernel: persistent, 128 x BN tiles of C (192 threads per CTA; as
+// many CTAs as fit on the SMs at once: one for BN = 256 and 128, two for 64).
 //   - one thread streams 128 x 64 tiles of A and BN x 64 tiles of B by TMA
 //     (128-byte swizzle) through a 4-stage ring;
 //   - one thread issues tcgen05.mma kind::f16 (M = 128, N = BN, K = 16, four
-//     per 64-wide K step) into a BN-column fp32 accumulator in tensor memory
-//     and frees each stage with tcgen05.commit;
-//   - all four warps then read their 32 accumulator lanes (rows) back with
-//     tcgen05.ld and store them, converted, with 16-byte stores.
+//     per 64-wide K step) into one of two BN-column fp32 accumulators in
+//     tensor memory and frees each stage with tcgen05.commit;
+//   - four epilogue warps read a finished accumulator's lanes (rows) back with
+//     tcgen05.ld and store them, converted, with 16-byte stores, while the
+//     next tile accumulates into the other half.
 // Rows past M and columns past N are zero-filled by TMA on load and masked on
 // store; a K that is not a multiple of 64 reads zeros past its end.
 //
@@ -38,7 +40,7 @@ namespace dsa {
 constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;
 constexpr int kGemmStages = 4;
-constexpr int kGemmThreads = 128;
+constexpr int kGemmThreads = 192;   // warp 0: TMA, warp 1: tensor memory and MMA, warps 2..5: epilogue
 
 template <int BN>
 struct GemmTc {
@@ -47,18 +49,21 @@ struct GemmTc {
     static constexpr int B_BYTES = BN * kGemmBK * 2;           // 8 .. 32 KB
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int OFF_BAR = kGemmStages * STAGE;
-    static constexpr int NBAR = 2 * kGemmStages + 1;           // full[S], empty[S], acc_full
+    static constexpr int NBAR = 2 * kGemmStages + 5;           // full[S], empty[S], acc_full[2], acc_empty[2], done
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;          // + alignment slack
     static constexpr uint32_t IDESC = idesc_bf16(kGemmBM, BN, false, false);
-    static constexpr int TMEM_COLS = BN;
+    static constexpr int TMEM_COLS = 2 * BN;                   // two accumulators
 };
 static_assert(GemmTc<256>::SMEM <= 232448, "gemm shared memory exceeds the per-CTA limit");
 static_assert(GemmTc<64>::STAGE % 1024 == 0 && GemmTc<128>::STAGE % 1024 == 0 && GemmTc<256>::STAGE % 1024 == 0,
               "stages hold 128B-swizzled tiles (1024-byte atoms)");
 
+// Persistent: CTA b takes tiles b, b + gridDim.x, ... of the (M / 128) x (N / BN) grid, N fastest
+// (neighbouring CTAs share the A rows in L2).  The accumulator alternates between two halves of
+// tensor memory, so the epilogue of one tile overlaps the MMAs of the next.
 template <int BN, bool OUT_BF16>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, int M, int N,
                int K, void* __restrict__ c, long long ldc, unsigned long long timeout_ns) {
     using G = GemmTc<BN>;
@@ -68,23 +73,27 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     const uint32_t bar0 = sbase + G::OFF_BAR;
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (kGemmStages + s); };
-    const uint32_t acc_full = bar0 + 8u * (2 * kGemmStages);
+    auto acc_full = [&](int a) { return bar0 + 8u * (2 * kGemmStages + a); };
+    auto acc_empty = [&](int a) { return bar0 + 8u * (2 * kGemmStages + 2 + a); };
+    const uint32_t done_bar = bar0 + 8u * (2 * kGemmStages + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::OFF_MISC);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + G::OFF_MISC + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kGemmBM;
     const int nk = (K + kGemmBK - 1) / kGemmBK;
+    const int tiles_n = (N + BN - 1) / BN;
+    const int ntiles = tiles_n * ((M + kGemmBM - 1) / kGemmBM);
 
     if (tid == 0) {
         for (int s = 0; s < kGemmStages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
-        mbar_init(acc_full, 1);
+        for (int a = 0; a < 2; ++a) { mbar_init(acc_full(a), 1); mbar_init(acc_empty(a), 128); }
+        mbar_init(done_bar, 1);
         *s_abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
     }
-    if (warp == 0) {
+    if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), G::TMEM_COLS);
         tmem_relinquish();
     }
@@ -93,89 +102,118 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
         // ---------------- TMA producer ----------------
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kGemmStages;
-            if (!wait_bar(empty(s), ((kb / kGemmStages) & 1) ^ 1, timeout_ns, s_abort)) break;
-            const uint32_t st = sbase + static_cast<uint32_t>(s * G::STAGE);
-            mbar_expect_tx(full(s), G::STAGE);
-            tma_load_2d(st, &tm_a, kb * kGemmBK, m0, full(s));
-            tma_load_2d(st + G::A_BYTES, &tm_b, kb * kGemmBK, n0, full(s));
-        }
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer ----------------
-        bool ok = true;
-        for (int kb = 0; kb < nk && ok; ++kb) {
-            const int s = kb % kGemmStages;
-            ok = wait_bar(full(s), (kb / kGemmStages) & 1, timeout_ns, s_abort);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t st = sbase + static_cast<uint32_t>(s * G::STAGE);
-            const uint64_t da = sdesc_sw128(st, 16, 1024), db = sdesc_sw128(st + G::A_BYTES, 16, 1024);
-#pragma unroll
-            for (int kk = 0; kk < kGemmBK / 16; ++kk)
-                tc_mma_bf16(tmem, da + static_cast<uint64_t>((kk * 32) >> 4), db + static_cast<uint64_t>((kk * 32) >> 4),
-                            G::IDESC, (kb | kk) ? 1u : 0u);
-            tc_commit(empty(s));
-        }
-        tc_commit(acc_full);   // also on the abort path: the epilogue's wait then ends at once
-    }
-    __syncwarp();
-
-    // ---------------- epilogue: warp w reads accumulator lanes (rows) 32w .. 32w+31 ----------------
-    const bool acc_ok = wait_bar(acc_full, 0, timeout_ns, s_abort) && *s_abort == 0;
-    if (__all_sync(0xffffffffu, acc_ok)) {
-        tc_fence_after();
-        const int row = m0 + warp * 32 + lane;
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(taddr + static_cast<uint32_t>(c0), v);
-            tmem_ld_wait();
-            const int col = n0 + c0;
-            if (row >= M || col >= N) continue;
-            const bool whole = col + 32 <= N;
-            if constexpr (OUT_BF16) {
-                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(c) + static_cast<long long>(row) * ldc + col;
-                if (whole) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t pk[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]),
-                                                                           __uint_as_float(v[8 * q + 2 * e + 1]));
-                            pk[e] = *reinterpret_cast<const uint32_t*>(&h);
-                        }
-                        reinterpret_cast<uint4*>(dst)[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < N - col) dst[j] = __float2bfloat16_rn(__uint_as_float(v[j]));
-                }
-            } else {
-                float* dst = static_cast<float*>(c) + static_cast<long long>(row) * ldc + col;
-                if (whole) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        reinterpret_cast<float4*>(dst)[q] =
-                            make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                        __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < N - col) dst[j] = __uint_as_float(v[j]);
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const int n0 = (t % tiles_n) * BN, m0 = (t / tiles_n) * kGemmBM;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % kGemmStages;
+                    ok = wait_bar(empty(s), ((it / kGemmStages) & 1) ^ 1, timeout_ns, s_abort);
+                    if (!ok) break;
+                    const uint32_t st = sbase + static_cast<uint32_t>(s * G::STAGE);
+                    mbar_expect_tx(full(s), G::STAGE);
+                    tma_load_2d(st, &tm_a, kb * kGemmBK, m0, full(s));
+                    tma_load_2d(st + G::A_BYTES, &tm_b, kb * kGemmBK, n0, full(s));
                 }
             }
+            if (!ok) sleep_ns(1000000ull);   // loads already issued land before the CTA exits
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            int it = 0, ti = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++ti) {
+                const int a = ti & 1;
+                // the epilogue has read this accumulator's previous tile
+                ok = wait_bar(acc_empty(a), ((ti >> 1) & 1) ^ 1, timeout_ns, s_abort);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(a * BN);
+                for (int kb = 0; kb < nk && ok; ++kb, ++it) {
+                    const int s = it % kGemmStages;
+                    ok = wait_bar(full(s), (it / kGemmStages) & 1, timeout_ns, s_abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t st = sbase + static_cast<uint32_t>(s * G::STAGE);
+                    const uint64_t da = sdesc_sw128(st, 16, 1024), db = sdesc_sw128(st + G::A_BYTES, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kGemmBK / 16; ++kk)
+                        tc_mma_bf16(d, da + static_cast<uint64_t>((kk * 32) >> 4),
+                                    db + static_cast<uint64_t>((kk * 32) >> 4), G::IDESC, (kb | kk) ? 1u : 0u);
+                    tc_commit(empty(s));
+                }
+                if (ok) tc_commit(acc_full(a));
+            }
+            tc_commit(done_bar);                          // every MMA issued has completed
+            wait_bar(done_bar, 0, timeout_ns, nullptr);   // before tensor memory is released
+        }
+    } else {
+        // ---------------- epilogue: warp w reads accumulator lanes (rows) 32 (w % 4) .. +31 ----------------
+        const int quad = warp & 3;
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        int ti = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++ti) {
+            const int a = ti & 1;
+            ok = __all_sync(0xffffffffu, wait_bar(acc_full(a), (ti >> 1) & 1, timeout_ns, s_abort));
+            if (!ok) break;
+            tc_fence_after();
+            const int n0 = (t % tiles_n) * BN, m0 = (t / tiles_n) * kGemmBM;
+            const int row = m0 + quad * 32 + lane;
+            const uint32_t taddr = tmem + lane_off + static_cast<uint32_t>(a * BN);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(taddr + static_cast<uint32_t>(c0), v);
+                tmem_ld_wait();
+                const int col = n0 + c0;
+                if (row >= M || col >= N) continue;
+                const bool whole = col + 32 <= N;
+                if constexpr (OUT_BF16) {
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(c) + static_cast<long long>(row) * ldc + col;
+                    if (whole) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]),
+                                                                               __uint_as_float(v[8 * q + 2 * e + 1]));
+                                pk[e] = *reinterpret_cast<const uint32_t*>(&h);
+                            }
+                            reinterpret_cast<uint4*>(dst)[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < N - col) dst[j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    }
+                } else {
+                    float* dst = static_cast<float*>(c) + static_cast<long long>(row) * ldc + col;
+                    if (whole) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            reinterpret_cast<float4*>(dst)[q] =
+                                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < N - col) dst[j] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(acc_empty(a));   // the MMA thread may start the tile after next in this half
         }
     }
-    if (*s_abort) sleep_ns(1000000ull);   // loads already issued land before the CTA exits
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, G::TMEM_COLS);
     }
