@@ -266,7 +266,8 @@ int dsa_index_scores_fp8_decode(const dsa_params* params, const void* q8, const 
  * int32 [batch, max_pages]) at offset s % page_size.  page_size is a power of
  * two in [128, 2^20] (a 128-key indexer tile never crosses a page), num_pages *
  * page_size <= 2^31 - 1, max_pages * page_size <= 2^20.  A page index outside
- * [0, num_pages) is read as page 0 and raises DSA_ERR_DEVICE_DATA.
+ * [0, num_pages) raises DSA_ERR_DEVICE_DATA: the decode reads page 0 in its
+ * place, and the append writes nothing for that sequence.
  * dsa_forward_decode_paged: dsa_forward_decode over paged caches, with
  *   max_ctx = max_pages * page_size (the score rows, the workspace size of
  *   dsa_decode_workspace_size(params, batch, max_ctx) and the selected

@@ -26,8 +26,9 @@
 //
 // update_indexer_kernel: one CTA per sequence copies the new token's indexer
 // key and latent row to position cache_seqlens[b] of its caches (dense, or
-// paged through a block table) and advances the length.  A length outside [0, max_ctx) (no room) writes nothing and
-// raises DSA_ERR_DEVICE_DATA.
+// paged through a block table) and advances the length.  A length outside
+// [0, max_ctx) (no room) or a page outside the pool writes nothing and raises
+// DSA_ERR_DEVICE_DATA.
 #pragma once
 
 #include <cuda.h>
@@ -232,11 +233,19 @@ update_indexer_kernel(RowSpec rs, const uint8_t* __restrict__ k_new, const uint8
     const int b = blockIdx.x;
     if (b >= rs.batch) return;
     const int p = cache_seqlens[b];
-    if (p < 0 || p >= rs.max_len) {   // no room (or a corrupt length): nothing is written
+    bool ok = p >= 0 && p < rs.max_len;   // else no room (or a corrupt length)
+    long long slot = static_cast<long long>(b) * rs.max_len + p;
+    if (ok && rs.pages != nullptr) {
+        // a page outside the pool is reported and nothing is written (the readers' fallback to
+        // page 0 would overwrite another sequence's rows here)
+        const int pg = __ldg(rs.pages + static_cast<long long>(b) * rs.max_pages + (p >> rs.page_log2));
+        ok = pg >= 0 && pg < rs.num_pages;
+        slot = (static_cast<long long>(pg) << rs.page_log2) + (p & ((1 << rs.page_log2) - 1));
+    }
+    if (!ok) {
         if (threadIdx.x == 0) raise_error(DSA_ERR_DEVICE_DATA);
         return;
     }
-    const long long slot = key_row(rs, b, static_cast<long long>(b) * rs.max_len, p);
     const uint4* ks = reinterpret_cast<const uint4*>(k_new + static_cast<long long>(b) * k_bytes);
     uint4* kd = reinterpret_cast<uint4*>(idx_cache + slot * k_bytes);
     for (int i = threadIdx.x; i < k_bytes / 16; i += kUpdThreads) kd[i] = ks[i];

@@ -135,3 +135,22 @@ def test_bad_page_index_is_reported_not_faulted():
                                128, bad.to(DEV), 3, torch.tensor([300, 200], dtype=torch.int32, device=DEV), 2, out,
                                None, None, ws, ws.numel())
     assert B.dsa_get_device_error() == B.DSA_ERR_DEVICE_DATA
+
+
+def test_paged_update_with_a_bad_page_writes_nothing():
+    cfg, p, num_pages, table, table_dev, idx_pool, kv_pool, *_ = _paged_problem("v32", [128, 5], 128, 2, 11)
+    bad = table_dev.clone()
+    bad[0, 1] = -3                                 # sequence 0's next position has no valid page
+    di, dkv = idx_pool.to(DEV), kv_pool.to(DEV)
+    lens = torch.tensor([128, 5], dtype=torch.int32, device=DEV)
+    g = torch.Generator().manual_seed(2)
+    k_new = torch.randn(2, cfg.idx_dim, generator=g).to(torch.bfloat16).to(DEV)
+    kv_new = torch.randn(2, cfg.d_qk, generator=g).to(torch.bfloat16).to(DEV)
+    B.dsa_update_indexer_paged(p, k_new, kv_new, 2, lens, di, dkv, num_pages, 128, bad.to(DEV), 2)
+    torch.cuda.synchronize()
+    assert B.dsa_get_device_error() == B.DSA_ERR_DEVICE_DATA
+    assert lens.cpu().tolist() == [128, 6]         # sequence 1 appended, sequence 0 not
+    pg1 = int(table[1, 0])
+    changed = (di != idx_pool.to(DEV)).any(dim=1).nonzero().flatten().tolist()
+    assert changed == [pg1 * 128 + 5]              # the one row of sequence 1, nothing else
+    assert torch.equal(di[pg1 * 128 + 5], k_new[1]) and torch.equal(dkv[pg1 * 128 + 5], kv_new[1])
