@@ -168,3 +168,26 @@ def test_update_then_decode_step():
                                               cfg.d_v)
         check_attention(out[b], ref_o)
         assert np.abs(lse[b] - ref_l).max() <= LSE_ABS
+
+
+def test_update_indexer_fp32_caches_are_bit_exact():
+    """The fp32 shape (4 x 32 indexer, 80-wide latent rows): the append copies bytes for either
+    dtype."""
+    cfg = CONFIGS["tiny"]
+    p = B.params_from_config(cfg)
+    Bn, M = 3, 17
+    g = torch.Generator().manual_seed(5)
+    idx = torch.randn(Bn, M, cfg.idx_dim, generator=g)
+    kv = torch.randn(Bn, M, cfg.d_qk, generator=g)
+    lens = torch.tensor([0, 9, 16], dtype=torch.int32)
+    k_new = torch.randn(Bn, cfg.idx_dim, generator=g)
+    kv_new = torch.randn(Bn, cfg.d_qk, generator=g)
+    ri, rkv, rl, full = O.update_indexer(idx.view(torch.int32).numpy(), kv.view(torch.int32).numpy(), lens.numpy(),
+                                         k_new.view(torch.int32).numpy(), kv_new.view(torch.int32).numpy())
+    di, dkv, dl = idx.to(DEV), kv.to(DEV), lens.to(DEV)
+    B.dsa_update_indexer(p, k_new.to(DEV), kv_new.to(DEV), Bn, M, dl, di, dkv)
+    torch.cuda.synchronize()
+    assert B.dsa_get_device_error() == B.DSA_OK and not full.any()
+    assert np.array_equal(dl.cpu().numpy(), rl)
+    assert np.array_equal(di.cpu().view(torch.int32).numpy(), ri)
+    assert np.array_equal(dkv.cpu().view(torch.int32).numpy(), rkv)
