@@ -1,4 +1,4 @@
-"""CPU oracle for the DeepSeek Sparse Attention (DSA) forward step.
+"""CPU oracle for the DeepSeek Sparse Attention (DSA) forward step and its backward.
 
 TEST INFRASTRUCTURE ONLY.  This module is the slow, plainly written
 definition that the CUDA library is checked against.  Only the test suite,
@@ -53,6 +53,10 @@ __all__ = [
     "masked_attention_row",
     "dsa_prefill",
     "dsa_decode",
+    "masked_attention_row_backward",
+    "sparse_attention_backward",
+    "index_scores_row_backward",
+    "index_scores_backward",
 ]
 
 _NEG_INF = -np.inf
@@ -439,3 +443,160 @@ def paged_to_dense(pool, block_table, page_size):
             if pg >= 0:
                 out[b, j * page_size:(j + 1) * page_size] = pool[pg * page_size:(pg + 1) * page_size]
     return out
+
+
+# ---------------------------------------------------------------------------
+# Backward of the path with the selection held fixed
+# ---------------------------------------------------------------------------
+# The "DeepSeek-V3.2" page calls DSA a trainable sparse attention.  The selection
+# (top-k of the index scores) is piecewise constant in the scores, so no gradient
+# flows through it; what is differentiable is the attention over the selected set
+# (step 4, for fixed idx) and the index scores themselves (step 1), at the
+# positions a loss reads them.  The pages give no training loss, so the gradients
+# of the outputs arrive as inputs.
+def masked_attention_row_backward(q_t, kv, mask_row, scale, d_v, dout, dlse=None):
+    """Gradient of ``masked_attention_row`` with respect to q_t and kv.
+
+    With the mask fixed the row is plain softmax attention.  For output gradients
+    dO [H, d_v] and (optionally) dlse [H]:
+
+        dP[h,s]  = dO[h,:] . kv[s,:d_v]
+        D[h]     = dO[h,:] . O[h,:]            (= sum_s p[h,s] dP[h,s])
+        dz[h,s]  = p[h,s] * (dP[h,s] - D[h] + dlse[h])
+        dq[h,:]  = scale * sum_s dz[h,s] kv[s,:]
+        dkv[s,:] = scale * sum_h dz[h,s] q[h,:],  plus sum_h p[h,s] dO[h,:] on the first d_v columns
+
+    (softmax Jacobian dp_s/dz_u = p_s (1[s=u] - p_u); d lse / d z_s = p_s).  Masked
+    positions have p = 0 and receive no gradient.
+
+    q_t [H, D_qk], kv [L, D_qk], mask_row [L], dout [H, d_v], dlse [H] or None
+    returns (dq [H, D_qk], dkv [L, D_qk]) float64
+    """
+    q = _f64(q_t)
+    k = _f64(kv)
+    g = _f64(dout)
+    z = scale * (q @ k.T) + mask_row[None, :]
+    zmax = np.max(z, axis=1, keepdims=True)
+    e = np.exp(z - zmax)
+    p = e / np.sum(e, axis=1, keepdims=True)       # [H, L]
+    v = k[:, :d_v]
+    out = p @ v                                    # [H, d_v]
+    dp = g @ v.T                                   # [H, L]
+    dd = np.sum(g * out, axis=1)                   # [H]
+    dz = dp - dd[:, None]
+    if dlse is not None:
+        dz = dz + _f64(dlse)[:, None]
+    dz = p * dz
+    dq = scale * (dz @ k)
+    dkv = scale * (dz.T @ q)
+    dkv[:, :d_v] += p.T @ g
+    return dq, dkv
+
+
+def sparse_attention_backward(q, kv, idx, cu_seqlens, scale, d_v, dout, dlse=None, rows=None):
+    """Backward of step 4 over a packed batch, for the selection ``idx`` held fixed.
+
+    q [T, H, D_qk], kv [T, D_qk], idx [T, k] sequence-local positions (-1 = empty),
+    cu_seqlens [B+1], dout [T, H, d_v], dlse [T, H] or None.
+
+    rows: the rows whose output gradients are taken (default: all); the gradients
+    of the other rows' outputs count as zero, so they add nothing to dkv.
+
+    Returns a dict with
+      rows [R] int64, dq [R, H, D_qk] float64 (the listed rows' query gradients),
+      dkv [T, D_qk] float64 (every row of every sequence, summed over the queries
+      that selected it).
+    """
+    cu = [int(c) for c in np.asarray(cu_seqlens).reshape(-1)]
+    T = cu[-1]
+    if rows is None:
+        rows = range(T)
+    rows = [int(r) for r in rows]
+    seq_of = np.searchsorted(np.asarray(cu), np.asarray(rows, dtype=np.int64), side="right") - 1
+    H, dqk = q.shape[1], q.shape[2]
+    idx = np.asarray(idx)
+    dq = np.zeros((len(rows), H, dqk))
+    dkv = np.zeros((T, dqk))
+    cache = {}
+    for i, (r, b) in enumerate(zip(rows, seq_of)):
+        b = int(b)
+        lo, hi = cu[b], cu[b + 1]
+        if b not in cache:
+            cache = {b: _f64(kv[lo:hi])}
+        kv_seq = cache[b]
+        mask = additive_mask_row(idx[r], hi - lo)
+        dl = None if dlse is None else _f64(dlse[r])
+        g_q, g_kv = masked_attention_row_backward(_f64(q[r]), kv_seq, mask, scale, d_v, _f64(dout[r]), dl)
+        dq[i] = g_q
+        dkv[lo:hi] += g_kv
+    return {"rows": np.asarray(rows, dtype=np.int64), "dq": dq, "dkv": dkv}
+
+
+def index_scores_row_backward(q_idx_t, w_t, k_idx_prefix, positions, d_scores):
+    """Gradient of ``index_scores_row`` read at the listed positions.
+
+    For  I[s] = sum_j w[j] * max(0, S[j,s]),  S[j,s] = q[j,:].k[s,:],  and a loss with
+    gradient g[m] on I[positions[m]]:
+
+        dw[j]   = sum_m g[m] * max(0, S[j,s_m])
+        G[j,m]  = g[m] * w[j] * [S[j,s_m] > 0]
+        dq[j,:] = sum_m G[j,m] k[s_m,:]
+        dk[s,:] = sum_{m: s_m = s} sum_j G[j,m] q[j,:]
+
+    The ReLU's derivative at exactly 0 is read as 0 (max(0, x) grows only for x > 0).
+    Entries with positions[m] < 0 are empty and contribute nothing.
+
+    q_idx_t [H_I, D_I], w_t [H_I], k_idx_prefix [n, D_I], positions [m], d_scores [m]
+    returns (dq [H_I, D_I], dw [H_I], dk [n, D_I]) float64
+    """
+    q = _f64(q_idx_t)
+    w = _f64(w_t)
+    k = _f64(k_idx_prefix)
+    pos = np.asarray(positions, dtype=np.int64).reshape(-1)
+    g = _f64(d_scores).reshape(-1)
+    keep = pos >= 0
+    pos, g = pos[keep], g[keep]
+    ks = k[pos]                                    # [m, D_I]
+    s = q @ ks.T                                   # [H_I, m]
+    dw = np.maximum(s, 0.0) @ g
+    G = (s > 0.0) * w[:, None] * g[None, :]
+    dq = G @ ks
+    dk = np.zeros_like(k)
+    np.add.at(dk, pos, G.T @ q)
+    return dq, dw, dk
+
+
+def index_scores_backward(q_idx, w, k_idx, idx, d_scores, cu_seqlens, rows=None):
+    """Backward of step 1 over a packed batch, the scores read at ``idx``.
+
+    q_idx [T, H_I, D_I], w [T, H_I], k_idx [T, D_I], idx [T, k] sequence-local
+    positions (-1 = empty), d_scores [T, k] the gradient at each listed position,
+    cu_seqlens [B+1].  rows: rows whose scores carry a gradient (default: all).
+
+    Returns a dict with rows [R], dq [R, H_I, D_I], dw [R, H_I] and dk [T, D_I]
+    (summed over every query that reads the key), float64.
+    """
+    cu = [int(c) for c in np.asarray(cu_seqlens).reshape(-1)]
+    T = cu[-1]
+    if rows is None:
+        rows = range(T)
+    rows = [int(r) for r in rows]
+    seq_of = np.searchsorted(np.asarray(cu), np.asarray(rows, dtype=np.int64), side="right") - 1
+    HI, DI = q_idx.shape[1], q_idx.shape[2]
+    idx = np.asarray(idx)
+    dq = np.zeros((len(rows), HI, DI))
+    dw = np.zeros((len(rows), HI))
+    dk = np.zeros((T, DI))
+    cache = {}
+    for i, (r, b) in enumerate(zip(rows, seq_of)):
+        b = int(b)
+        lo, hi = cu[b], cu[b + 1]
+        if b not in cache:
+            cache = {b: _f64(k_idx[lo:hi])}
+        t = r - lo
+        g_q, g_w, g_k = index_scores_row_backward(_f64(q_idx[r]), _f64(w[r]), cache[b][: t + 1], idx[r],
+                                                  _f64(d_scores[r]))
+        dq[i] = g_q
+        dw[i] = g_w
+        dk[lo:lo + t + 1] += g_k
+    return {"rows": np.asarray(rows, dtype=np.int64), "dq": dq, "dw": dw, "dk": dk}
