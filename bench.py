@@ -817,7 +817,126 @@ def run_inputs(args, cfg):
         "roofline": {"bound": "tensor", "kernel": "gemm_tc_kernel<256,true>", "achieved": tf[0],
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": tf[0] / peaks["bf16_tflops"],
                      "peak_kind": f"bf16 dense, burst, {peaks['source']}"},
-        "clocks": clocks, "gpu_launches": 4,
+        "clocks": clocks, "gpu_launches": 4 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def flop_per_pair_attn_bwd(cfg):
+    """Attention-backward flop per selected (t, s) pair: the logits q.k (d_qk) and dP = dO.v (d_v)
+    recomputed, dq += dz.kv (d_qk), dkv += dz.q (d_qk) + p.dO (d_v), for each head (704,512 at
+    128 heads, 576 / 512)."""
+    return 2 * cfg.n_heads * (3 * cfg.d_qk + 2 * cfg.d_v)
+
+
+def flop_per_pair_idx_bwd(cfg):
+    """Index-score-backward flop per listed (t, s) pair: S = q_I.k_I, dq_I += G.k_I and
+    dk_I += G.q_I for each indexer head (49,152 at 64 x 128)."""
+    return 3 * 2 * cfg.n_idx_heads * cfg.idx_dim
+
+
+def run_backward(args, cfg):
+    """Backward of the path with the selection fixed (training): the attention's dq and dkv and
+    the index scores' dq_I, dw, dk_I at the selected positions, for the output gradients of a
+    loss the pages do not give (seeded N(0, 1) inputs).  The selection, out and lse come from the
+    library's forward over the same inputs (untimed).  One JSON line with its own metric: the
+    two kernels' TFLOP/s against the CUDA cores' fp32 FMA peak (they run in fp32 on the CUDA
+    cores) and, for reference, the bf16 tensor peak."""
+    import torch
+
+    import sparse_attention_long_gemm_b300 as dsa
+    from sparse_attention_long_gemm_b300.build import build_library
+    from sparse_attention_long_gemm_b300.synth import make_backward_inputs, make_prefill_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build_library()
+    p = dsa.params_from_config(cfg)
+    inp = make_prefill_inputs(cfg, dev, seed=0)
+    lens = inp["lengths"]
+    T, B, maxL = sum(lens), len(lens), inp["max_seqlen"]
+    ld = (maxL + 3) // 4 * 4
+    _, selected = _work_counts(lens, cfg.topk)
+    scores = torch.empty((T, ld), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, cfg.topk), dtype=torch.int32, device=dev)
+    out = torch.empty((T, cfg.n_heads, cfg.d_v), dtype=inp["q"].dtype, device=dev)
+    lse = torch.empty((T, cfg.n_heads), dtype=torch.float32, device=dev)
+    cu = inp["cu_seqlens"]
+    dsa.dsa_index_scores(p, inp["q_idx"], inp["w"], inp["k_idx"], cu, B, T, maxL, scores, ld)
+    dsa.dsa_topk(p, scores, ld, cu, B, T, maxL, idx)
+    dsa.dsa_sparse_mla_attn(p, inp["q"], inp["kv"], idx, cu, B, T, maxL, out, lse)
+    del scores
+    bw = make_backward_inputs(cfg, T, dev, seed=0)
+    dq = torch.empty((T, cfg.n_heads, cfg.d_qk), dtype=torch.float32, device=dev)
+    dkv = torch.empty((T, cfg.d_qk), dtype=torch.float32, device=dev)
+    dqi = torch.empty((T, cfg.n_idx_heads, cfg.idx_dim), dtype=torch.float32, device=dev)
+    dwi = torch.empty((T, cfg.n_idx_heads), dtype=torch.float32, device=dev)
+    dki = torch.empty((T, cfg.idx_dim), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (126 MB)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        dsa.dsa_sparse_mla_attn_bwd(p, inp["q"], inp["kv"], idx, cu, B, T, maxL, out, lse, bw["dout"], bw["dlse"],
+                                    dq, dkv, sp)
+        if evs:
+            evs[1].record(stream)
+        dsa.dsa_index_scores_bwd(p, inp["q_idx"], inp["w"], inp["k_idx"], idx, bw["d_scores"], cu, B, T, maxL, dqi,
+                                 dwi, dki, sp)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if dsa.dsa_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks_dir = os.environ.get("DSA_CLOCKS_DIR") or tempfile.gettempdir()
+    sampler = ClockSampler(0, os.path.join(clocks_dir, "dsa_clocks_backward.csv"))
+    torch.cuda.synchronize(dev)
+    for s_ in range(args.steps):
+        flush.zero_()
+        step(evs[s_])
+    torch.cuda.synchronize(dev)
+    st = [[e[i].elapsed_time(e[i + 1]) for i in range(2)] for e in evs]
+    extra = clock_tail(step, flush, dev, [sum(x) for x in st])
+    clocks = sampler.stop()
+    if clocks is not None:
+        clocks["untimed_steps_after"] = extra
+    if dsa.dsa_get_device_error() != 0:
+        raise RuntimeError("device error during timing")
+    ms = [statistics.median(x[i] for x in st) for i in range(2)]
+    peaks = _peaks()
+    props = torch.cuda.get_device_properties(dev)
+    mhz = (clocks or {}).get("sm_max_mhz") or 2032.0
+    # fp32 FMA peak of the CUDA cores: 128 lanes per SM, 2 flop per FMA, at the maximum SM clock
+    alu_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+    fl = [selected * flop_per_pair_attn_bwd(cfg), selected * flop_per_pair_idx_bwd(cfg)]
+    tf = [f / (m * 1e9) for f, m in zip(fl, ms)]
+    line = {
+        "metric": "DSA backward (selection fixed) TFLOP/s: sparse attention + index scores",
+        "value": sum(fl) / (sum(ms) * 1e9), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sum(ms), "higher_is_better": True, "dtype": "f32 (bf16 inputs)",
+        "data": "synthetic",
+        "config": {"workload": _workload_desc(cfg, lens) + f"; {selected} selected pairs",
+                   "l2": "flushed (256 MB write) between timed steps", "timing": f"median of {args.steps} steps"},
+        "stages": {
+            "sparse_mla_attn_bwd": {"ms": ms[0], "tflops": tf[0], "flop_per_pair": flop_per_pair_attn_bwd(cfg),
+                                    "frac_of_alu_peak": tf[0] / alu_peak,
+                                    "frac_of_bf16_peak": tf[0] / peaks["bf16_tflops"]},
+            "index_scores_bwd": {"ms": ms[1], "tflops": tf[1], "flop_per_pair": flop_per_pair_idx_bwd(cfg),
+                                 "frac_of_alu_peak": tf[1] / alu_peak,
+                                 "frac_of_bf16_peak": tf[1] / peaks["bf16_tflops"]},
+        },
+        "roofline": {"bound": "alu", "kernel": "attn_bwd_kernel<bf16>", "achieved": tf[0], "peak": alu_peak,
+                     "unit": "TFLOP/s", "frac": tf[0] / alu_peak,
+                     "peak_kind": f"fp32 FMA on the CUDA cores: {props.multi_processor_count} SMs x 128 lanes x 2 "
+                                  f"flop x {mhz:.0f} MHz"},
+        "clocks": clocks, "gpu_launches": 4 * args.steps,   # two zero fills and the two backward kernels
     }
     print(json.dumps(line), flush=True)
 
@@ -832,8 +951,9 @@ def main():
     ap.add_argument("--seqlen", type=int, default=0, help="override: one prefill sequence of this length")
     ap.add_argument("--indexer", default="native", choices=["native", "fp8"],
                     help="fp8: the indexer's FP8 form (rotation + E4M3 codes) in place of bf16")
-    ap.add_argument("--stage", default="forward", choices=["forward", "inputs"],
-                    help="inputs: time the indexer's input projections and the cache append instead")
+    ap.add_argument("--stage", default="forward", choices=["forward", "inputs", "backward"],
+                    help="inputs: time the indexer's input projections and the cache append instead; "
+                         "backward: time the backward calls (selection fixed)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=24)
@@ -850,6 +970,8 @@ def main():
         cfg = scaled(cfg, seqlens=(args.seqlen,), varlen_range=())
     if args.stage == "inputs":
         run_inputs(args, cfg)
+    elif args.stage == "backward":
+        run_backward(args, cfg)
     elif args.impl == "reference":
         run_reference(args, cfg)
     else:

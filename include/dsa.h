@@ -293,6 +293,52 @@ int dsa_update_indexer(const dsa_params* params, const void* k_new, const void* 
                        int max_ctx, int* cache_seqlens, void* idx_cache, void* kv_cache,
                        void* stream);
 
+/* ---- Backward (training): gradients with the selection held fixed ----
+ * DeepSeek-V3.2 page, overview: DSA is a trainable sparse attention.  The
+ * top-k selection is piecewise constant in the scores, so no gradient passes
+ * through it; the differentiable parts are the attention over the selected
+ * positions and the index scores themselves.  The pages give no loss, so the
+ * gradients of the outputs are inputs.  Both calls run on the CUDA cores in
+ * fp32, accumulate the key-side gradients with fp32 atomic adds (so their
+ * summation order, and the last bits, vary from run to run), and write fp32
+ * gradients.  Packed prefill batches only (cu_seqlens as in the forward).
+ *
+ * dsa_sparse_mla_attn_bwd: backward of dsa_sparse_mla_attn for the same idx.
+ *   q, kv, idx, cu_seqlens as in the forward; out [total_q, n_heads, d_v] and
+ *   lse [total_q, n_heads] (required) are the forward's outputs for them;
+ *   dout [total_q, n_heads, d_v] (dtype) the output gradient; dlse
+ *   [total_q, n_heads] fp32 the lse gradient, or NULL for none.  Writes
+ *     dq  [total_q, n_heads, d_qk] fp32 = scale * sum_i dz[h,i] kv[s_i,:]
+ *     dkv [total_q, d_qk] fp32 (overwritten) = sum over the queries that
+ *         selected row s of scale * sum_h dz[h,i] q[h,:], plus
+ *         sum_h p[h,i] dO[h,:] on the first d_v columns,
+ *   where p = exp(scale q.kv - lse) and dz = p (dO.kv[:d_v] - dO.O + dlse).
+ *   Entries of idx outside [0, t] other than -1 are skipped and raise
+ *   DSA_ERR_DEVICE_DATA; positions must be distinct, as in the forward.
+ *   d_qk <= 640 and the CTA's shared tiles within 227 KB, else
+ *   DSA_ERR_UNSUPPORTED.  All pointers 16-byte aligned device memory.
+ * dsa_index_scores_bwd: backward of dsa_index_scores read at listed positions.
+ *   q_idx, w, k_idx as in dsa_index_scores; idx [total_q, topk] int32
+ *   sequence-local positions (-1 = empty; topk = params->topk per row, e.g.
+ *   the selection, or every position 0..t for the whole causal row) and
+ *   d_scores [total_q, topk] fp32 the gradient at each listed position.  Writes
+ *     dq_idx [total_q, n_idx_heads, idx_dim] fp32, dw [total_q, n_idx_heads]
+ *     fp32, dk_idx [total_q, idx_dim] fp32 (overwritten),
+ *   with G[j,m] = d_scores[m] * w[j] * [q_idx[j].k_idx[s_m] > 0] (the ReLU's
+ *   decision taken on the fp32 dot product): dw[j] = sum_m d_scores[m] *
+ *   ReLU(q_idx[j].k_idx[s_m]), dq_idx[j] = sum_m G[j,m] k_idx[s_m],
+ *   dk_idx[s] = sum over (row, m) listing s of sum_j G[j,m] q_idx[j].
+ *   n_idx_heads <= 64 and idx_dim <= 128, else DSA_ERR_UNSUPPORTED.  Bad
+ *   positions as above.  All pointers 16-byte aligned device memory. */
+int dsa_sparse_mla_attn_bwd(const dsa_params* params, const void* q, const void* kv,
+                            const int* idx, const int* cu_seqlens, int batch, int total_q,
+                            int max_seqlen, const void* out, const float* lse, const void* dout,
+                            const float* dlse, float* dq, float* dkv, void* stream);
+int dsa_index_scores_bwd(const dsa_params* params, const void* q_idx, const float* w,
+                         const void* k_idx, const int* idx, const float* d_scores,
+                         const int* cu_seqlens, int batch, int total_q, int max_seqlen,
+                         float* dq_idx, float* dw, float* dk_idx, void* stream);
+
 /* Synchronises `stream`, then returns and clears the device error word:
  * DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_DATA (DSA_ERR_CUDA if the
  * synchronisation itself failed). */

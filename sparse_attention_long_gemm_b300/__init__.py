@@ -1,4 +1,4 @@
-"""DeepSeek Sparse Attention (DSA) forward step on one B300 (sm_103a).
+"""DeepSeek Sparse Attention (DSA) forward step and its backward on one B300 (sm_103a).
 
 The compute lives in libdsa.so (CUDA kernels behind the C ABI of
 include/dsa.h).  This package holds its ctypes binding (``_binding``: the C
@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     dsa_gemm_bf16,
     dsa_get_device_error,
     dsa_index_scores,
+    dsa_index_scores_bwd,
     dsa_index_scores_decode,
     dsa_index_scores_fp8,
     dsa_index_scores_fp8_decode,
@@ -34,6 +35,7 @@ from ._binding import (  # noqa: F401
     dsa_selftest_wait_timeout,
     dsa_set_wait_timeout_ns,
     dsa_sparse_mla_attn,
+    dsa_sparse_mla_attn_bwd,
     dsa_sparse_mla_attn_decode,
     dsa_topk,
     dsa_topk_decode,
@@ -92,6 +94,33 @@ def sparse_mla_attn(p, q, kv, idx, cu_seqlens, max_seqlen, want_lse=True, stream
     lse = torch.empty((T, p.n_heads), dtype=torch.float32, device=q.device) if want_lse else None
     dsa_sparse_mla_attn(p, q, kv, idx, cu_seqlens, cu_seqlens.numel() - 1, T, max_seqlen, out, lse, stream)
     return out, lse
+
+
+def sparse_mla_attn_bwd(p, q, kv, idx, cu_seqlens, max_seqlen, out, lse, dout, dlse=None, stream=None):
+    """Gradients of the sparse attention for the selection idx: (dq [T, H, d_qk], dkv [T, d_qk]), fp32."""
+    import torch
+
+    T = q.shape[0]
+    dq = torch.empty((T, p.n_heads, p.d_qk), dtype=torch.float32, device=q.device)
+    dkv = torch.empty((T, p.d_qk), dtype=torch.float32, device=q.device)
+    dsa_sparse_mla_attn_bwd(p, q, kv, idx, cu_seqlens, cu_seqlens.numel() - 1, T, max_seqlen, out, lse, dout, dlse,
+                            dq, dkv, stream)
+    return dq, dkv
+
+
+def index_scores_bwd(p, q_idx, w, k_idx, idx, d_scores, cu_seqlens, max_seqlen, stream=None):
+    """Gradients of the index scores read at idx [T, p.topk] with gradient d_scores [T, p.topk]:
+    (dq_idx [T, H_I, D_I], dw [T, H_I], dk_idx [T, D_I]), fp32."""
+    import torch
+
+    T = q_idx.shape[0]
+    dev = q_idx.device
+    dq = torch.empty((T, p.n_idx_heads, p.idx_dim), dtype=torch.float32, device=dev)
+    dw = torch.empty((T, p.n_idx_heads), dtype=torch.float32, device=dev)
+    dk = torch.empty((T, p.idx_dim), dtype=torch.float32, device=dev)
+    dsa_index_scores_bwd(p, q_idx, w, k_idx, idx, d_scores, cu_seqlens, cu_seqlens.numel() - 1, T, max_seqlen,
+                         dq, dw, dk, stream)
+    return dq, dw, dk
 
 
 def prefill(p, q_idx, w, k_idx, q, kv, cu_seqlens, max_seqlen, want_lse=True, want_idx=False,

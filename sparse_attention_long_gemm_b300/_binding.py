@@ -51,6 +51,8 @@ EXPORTED = [
     "dsa_update_indexer",
     "dsa_forward_decode_paged",
     "dsa_update_indexer_paged",
+    "dsa_sparse_mla_attn_bwd",
+    "dsa_index_scores_bwd",
 ]
 
 
@@ -130,6 +132,10 @@ def lib():
         L.dsa_update_indexer_paged.argtypes = [P, vp, vp, i, vp, vp, vp, i, i, vp, i, vp]
         L.dsa_update_indexer.restype = i
         L.dsa_update_indexer.argtypes = [P, vp, vp, i, i, vp, vp, vp, vp]
+        L.dsa_sparse_mla_attn_bwd.restype = i
+        L.dsa_sparse_mla_attn_bwd.argtypes = [P, vp, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp, vp, vp]
+        L.dsa_index_scores_bwd.restype = i
+        L.dsa_index_scores_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, i, i, i, vp, vp, vp, vp]
         L.dsa_get_device_error.restype = i
         L.dsa_get_device_error.argtypes = [vp]
         L.dsa_set_wait_timeout_ns.restype = ll
@@ -300,6 +306,22 @@ def dsa_update_indexer_paged(p, k_new, kv_new, batch, cache_seqlens, idx_pool, k
                                         _ptr(idx_pool), _ptr(kv_pool), num_pages, page_size, _ptr(block_table),
                                         max_pages, _stream(stream))
     _check(rc, "dsa_update_indexer_paged")
+
+
+def dsa_sparse_mla_attn_bwd(p, q, kv, idx, cu_seqlens, batch, total_q, max_seqlen, out, lse, dout, dlse, dq, dkv,
+                            stream=None):
+    rc = lib().dsa_sparse_mla_attn_bwd(ctypes.byref(p), _ptr(q), _ptr(kv), _ptr(idx), _ptr(cu_seqlens), batch,
+                                       total_q, max_seqlen, _ptr(out), _ptr(lse), _ptr(dout), _ptr(dlse), _ptr(dq),
+                                       _ptr(dkv), _stream(stream))
+    _check(rc, "dsa_sparse_mla_attn_bwd")
+
+
+def dsa_index_scores_bwd(p, q_idx, w, k_idx, idx, d_scores, cu_seqlens, batch, total_q, max_seqlen, dq_idx, dw,
+                         dk_idx, stream=None):
+    rc = lib().dsa_index_scores_bwd(ctypes.byref(p), _ptr(q_idx), _ptr(w), _ptr(k_idx), _ptr(idx), _ptr(d_scores),
+                                    _ptr(cu_seqlens), batch, total_q, max_seqlen, _ptr(dq_idx), _ptr(dw),
+                                    _ptr(dk_idx), _stream(stream))
+    _check(rc, "dsa_index_scores_bwd")
 
 
 def dsa_get_device_error(stream=None) -> int:

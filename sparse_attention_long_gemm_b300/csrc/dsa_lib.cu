@@ -14,9 +14,11 @@
 #include <cstdio>
 #include <mutex>
 
+#include "attn_bwd.cuh"
 #include "attn_simt.cuh"
 #include "attn_tc.cuh"
 #include "gemm_tc.cuh"
+#include "indexer_bwd.cuh"
 #include "indexer_fp8.cuh"
 #include "indexer_simt.cuh"
 #include "indexer_tc.cuh"
@@ -34,6 +36,9 @@ constexpr int kPreNQ = 4, kPreKS = 3, kPreQB = 2, kPreKC = 32;
 constexpr int kDecNQ = 1, kDecKS = 5, kDecQB = 2, kDecKC = 8;
 // FP8 forms: tiles are half the bytes, so more key stages fit
 constexpr int kF8PreKS = 6, kF8DecKS = 8;
+
+// largest dynamic shared memory a CTA may ask for (227 KB)
+constexpr size_t kMaxDynSmem = 232448;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
@@ -73,6 +78,7 @@ int launch_status() { return cuda_status(cudaGetLastError()); }
 
 struct DevInfo {
     int sm_count = 0;
+    size_t max_smem = 0;   // dynamic shared memory a CTA may opt into
     bool attrs_set = false;
 };
 std::mutex g_mu;
@@ -111,6 +117,15 @@ int device_info(DevInfo** out) {
         set(reinterpret_cast<const void*>(&indexer_simt_kernel<__nv_bfloat16>), indexer_simt_smem(128, 128));
         set(reinterpret_cast<const void*>(&attn_simt_kernel<float>), attn_simt_smem(1024, 16384));
         set(reinterpret_cast<const void*>(&attn_simt_kernel<__nv_bfloat16>), attn_simt_smem(1024, 16384));
+        int optin = 0;
+        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        d.max_smem = std::min(static_cast<size_t>(optin), kMaxDynSmem);
+        set(reinterpret_cast<const void*>(&attn_bwd_kernel<float>), d.max_smem);
+        set(reinterpret_cast<const void*>(&attn_bwd_kernel<__nv_bfloat16>), d.max_smem);
+        set(reinterpret_cast<const void*>(&index_scores_bwd_kernel<float>), IbSmem<float>(kIbMaxDim).bytes);
+        set(reinterpret_cast<const void*>(&index_scores_bwd_kernel<__nv_bfloat16>),
+            IbSmem<__nv_bfloat16>(kIbMaxDim).bytes);
         if (e != cudaSuccess) return DSA_ERR_CUDA;
         d.attrs_set = true;
     }
@@ -369,6 +384,62 @@ int run_attn(const dsa_params* p, const void* q, const void* kv, const int* idx,
     return launch_status();
 }
 
+// dst[0 .. n) = 0 on the stream (n a multiple of 4)
+int run_zero(float* dst, long long n, cudaStream_t st) {
+    if (n <= 0) return DSA_OK;
+    DevInfo* di = nullptr;
+    int rc = device_info(&di);
+    if (rc != DSA_OK) return rc;
+    const long long blocks = std::min<long long>((n / 4 + 255) / 256, 8LL * di->sm_count);
+    zero_f32_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(dst, n);
+    return launch_status();
+}
+
+// Backward of step 4 for packed prefill rows: dkv zeroed, then one CTA per (row, 32 heads).
+int run_attn_bwd(const dsa_params* p, const void* q, const void* kv, const int* idx, const RowSpec& rs, int rows,
+                 const void* out, const float* lse, const void* dout, const float* dlse, float* dq, float* dkv,
+                 cudaStream_t st) {
+    DevInfo* di = nullptr;
+    int rc = device_info(&di);
+    if (rc != DSA_OK) return rc;
+    const size_t sm = p->dtype == DSA_BF16 ? AbSmem<__nv_bfloat16>(p->d_qk, p->d_v).bytes
+                                           : AbSmem<float>(p->d_qk, p->d_v).bytes;
+    if (sm > di->max_smem) return DSA_ERR_UNSUPPORTED;
+    if ((rc = run_zero(dkv, static_cast<long long>(rows) * p->d_qk, st)) != DSA_OK) return rc;
+    const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>((p->n_heads + kAbHeads - 1) / kAbHeads));
+    if (p->dtype == DSA_BF16) {
+        using T = __nv_bfloat16;
+        attn_bwd_kernel<T><<<grid, kAbThreads, sm, st>>>(
+            rs, static_cast<const T*>(q), static_cast<const T*>(kv), idx, p->topk, p->n_heads, p->d_qk, p->d_v,
+            p->softmax_scale, static_cast<const T*>(out), lse, static_cast<const T*>(dout), dlse, dq, dkv, rows);
+    } else {
+        attn_bwd_kernel<float><<<grid, kAbThreads, sm, st>>>(
+            rs, static_cast<const float*>(q), static_cast<const float*>(kv), idx, p->topk, p->n_heads, p->d_qk,
+            p->d_v, p->softmax_scale, static_cast<const float*>(out), lse, static_cast<const float*>(dout), dlse, dq,
+            dkv, rows);
+    }
+    return launch_status();
+}
+
+// Backward of step 1 at listed positions for packed prefill rows: dk zeroed, then one CTA per row.
+int run_index_scores_bwd(const dsa_params* p, const void* q_idx, const float* w, const void* k_idx, const int* idx,
+                         const float* dsc, const RowSpec& rs, int rows, float* dq, float* dw, float* dk,
+                         cudaStream_t st) {
+    int rc = run_zero(dk, static_cast<long long>(rows) * p->idx_dim, st);
+    if (rc != DSA_OK) return rc;
+    if (p->dtype == DSA_BF16) {
+        using T = __nv_bfloat16;
+        index_scores_bwd_kernel<T><<<rows, kIbThreads, IbSmem<T>(p->idx_dim).bytes, st>>>(
+            rs, static_cast<const T*>(q_idx), w, static_cast<const T*>(k_idx), idx, dsc, p->topk, p->n_idx_heads,
+            p->idx_dim, dq, dw, dk, rows);
+    } else {
+        index_scores_bwd_kernel<float><<<rows, kIbThreads, IbSmem<float>(p->idx_dim).bytes, st>>>(
+            rs, static_cast<const float*>(q_idx), w, static_cast<const float*>(k_idx), idx, dsc, p->topk,
+            p->n_idx_heads, p->idx_dim, dq, dw, dk, rows);
+    }
+    return launch_status();
+}
+
 int check_prefill_common(const dsa_params* p, const int* cu, int batch, int total_q, int max_seqlen) {
     int rc = check_params(p);
     if (rc != DSA_OK) return rc;
@@ -618,6 +689,45 @@ int dsa_index_scores_fp8_decode(const dsa_params* params, const void* q8, const 
     const RowSpec rs{cache_seqlens, batch, 1, max_ctx};
     return run_index_scores_fp8(static_cast<const uint8_t*>(q8), wq, static_cast<const uint8_t*>(k8_cache), ksc_cache,
                                 rs, batch, static_cast<long long>(batch) * max_ctx, scores, ld,
+                                static_cast<cudaStream_t>(stream));
+}
+
+int dsa_sparse_mla_attn_bwd(const dsa_params* params, const void* q, const void* kv, const int* idx,
+                            const int* cu_seqlens, int batch, int total_q, int max_seqlen, const void* out,
+                            const float* lse, const void* dout, const float* dlse, float* dq, float* dkv,
+                            void* stream) {
+    int rc = check_prefill_common(params, cu_seqlens, batch, total_q, max_seqlen);
+    if (rc != DSA_OK) return rc;
+    if (q == nullptr || kv == nullptr || idx == nullptr || out == nullptr || lse == nullptr || dout == nullptr ||
+        dq == nullptr || dkv == nullptr)
+        return DSA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(idx) || !aligned16(out) || !aligned16(lse) ||
+        !aligned16(dout) || (dlse && !aligned16(dlse)) || !aligned16(dq) || !aligned16(dkv))
+        return DSA_ERR_ARG;
+    const size_t sm = params->dtype == DSA_BF16 ? AbSmem<__nv_bfloat16>(params->d_qk, params->d_v).bytes
+                                                : AbSmem<float>(params->d_qk, params->d_v).bytes;
+    if (params->d_qk > kAbMaxDqk || sm > kMaxDynSmem) return DSA_ERR_UNSUPPORTED;
+    if (total_q == 0) return DSA_OK;
+    const RowSpec rs{cu_seqlens, batch, 0, max_seqlen};
+    return run_attn_bwd(params, q, kv, idx, rs, total_q, out, lse, dout, dlse, dq, dkv,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int dsa_index_scores_bwd(const dsa_params* params, const void* q_idx, const float* w, const void* k_idx,
+                         const int* idx, const float* d_scores, const int* cu_seqlens, int batch, int total_q,
+                         int max_seqlen, float* dq_idx, float* dw, float* dk_idx, void* stream) {
+    int rc = check_prefill_common(params, cu_seqlens, batch, total_q, max_seqlen);
+    if (rc != DSA_OK) return rc;
+    if (q_idx == nullptr || w == nullptr || k_idx == nullptr || idx == nullptr || d_scores == nullptr ||
+        dq_idx == nullptr || dw == nullptr || dk_idx == nullptr)
+        return DSA_ERR_ARG;
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(idx) || !aligned16(d_scores) ||
+        !aligned16(dq_idx) || !aligned16(dw) || !aligned16(dk_idx))
+        return DSA_ERR_ARG;
+    if (params->n_idx_heads > kIbHeads || params->idx_dim > kIbMaxDim) return DSA_ERR_UNSUPPORTED;
+    if (total_q == 0) return DSA_OK;
+    const RowSpec rs{cu_seqlens, batch, 0, max_seqlen};
+    return run_index_scores_bwd(params, q_idx, w, k_idx, idx, d_scores, rs, total_q, dq_idx, dw, dk_idx,
                                 static_cast<cudaStream_t>(stream));
 }
 

@@ -148,3 +148,36 @@ def make_decode_inputs(cfg: DSAConfig, device="cpu", seed: int = 0):
         "lengths": lens,
         "max_ctx": cfg.max_ctx,
     }
+
+
+def random_selection(lengths, topk, seed: int = 0):
+    """A seeded selection of the shape the top-k step produces: for the query at position t
+    of each packed sequence, min(topk, t + 1) distinct positions of 0..t in ascending order,
+    padded with -1 to topk (every position when t + 1 <= topk, a uniform random subset
+    otherwise).  int32 [sum(lengths), topk] on the CPU."""
+    g = torch.Generator().manual_seed(seed + 7)
+    rows = []
+    for L in lengths:
+        for t in range(L):
+            n = t + 1
+            if n <= topk:
+                sel = torch.arange(n, dtype=torch.int32)
+            else:
+                sel = torch.randperm(n, generator=g)[:topk].sort().values.to(torch.int32)
+            row = torch.full((topk,), -1, dtype=torch.int32)
+            row[: sel.numel()] = sel
+            rows.append(row)
+    if not rows:
+        return torch.empty((0, topk), dtype=torch.int32)
+    return torch.stack(rows)
+
+
+def make_backward_inputs(cfg: DSAConfig, T: int, device="cpu", seed: int = 0):
+    """Gradients arriving at the forward's outputs (the pages give no loss): dout
+    [T, H, d_v] in the config's dtype, dlse [T, H] fp32, and a gradient on the index scores
+    d_scores [T, topk] fp32, all N(0, 1)."""
+    g = torch.Generator(device=device).manual_seed(seed + 11)
+    dout = _draw(g, (T, cfg.n_heads, cfg.d_v), 1.0, device).to(cfg.torch_dtype)
+    dlse = _draw(g, (T, cfg.n_heads), 1.0, device)
+    d_scores = _draw(g, (T, cfg.topk), 1.0, device)
+    return {"dout": dout, "dlse": dlse, "d_scores": d_scores}

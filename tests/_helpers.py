@@ -96,3 +96,66 @@ def sample_rows(cu, k, per_seq=8, seed=0):
         pos |= set(int(x) for x in rng.integers(0, L, size=per_seq))
         rows += [lo + t for t in sorted(pos) if 0 <= t < L]
     return rows
+
+
+# ---------------------------------------------------------------------------
+# Backward tolerances (per-element bounds derived from the arithmetic)
+# ---------------------------------------------------------------------------
+# fp32 arithmetic of the backward kernels: ETA bounds the relative error of a dot
+# product or a per-query sum of at most a few thousand terms (random-walk growth of
+# 2^-24 per operation, with a wide margin); ETA_ACC that of the key-side sums, which
+# add terms of every (query, head) that selected a key through fp32 atomics.
+BWD_ETA = 1e-5
+BWD_ETA_ACC = 1e-4
+# Error of the forward output O the backward reads, as a multiple of sum_i p_i |v_i|:
+# the tensor-core forward rounds the unnormalised probabilities to bf16 for P.V and O to
+# bf16 (2^-9 each); an O rounded once to bf16 is off by 2^-9 |O|; the fp32 forward by ~1e-6.
+O_REL_BF16_FORWARD = 2.0 ** -8
+O_REL_BF16_ROUNDED = 2.0 ** -9
+O_REL_FP32_FORWARD = 4e-6
+# A fp32 dot product of D_I bf16 products is off by at most (D_I - 1) 2^-24 sum |q k|;
+# decisions [S > 0] with |S| inside 2e-5 sum |q k| may fall either way.
+IDX_DECISION_REL = 2e-5
+
+
+def attn_bwd_bounds(q_t, kv_sel, scale, d_v, dout_t, dlse_t, o_rel):
+    """Error bounds of the GPU backward of one query row against the fp64 oracle.
+
+    q_t [H, D_qk], kv_sel [m, D_qk] (the selected rows), dout_t [H, d_v], dlse_t [H].
+    The gradient dz = p (dP - D + dlse) carries: the error of D = dO . O from the forward's
+    O (o_rel * sum_d |dO_d| sum_i p_i |v_id|) and the fp32 errors of dP, D and p (ETA times
+    the absolute sums).  dq and dkv add the fp32 error of their own sums.
+    Returns (bound_dq [H, D_qk], bound_dkv [m, D_qk])."""
+    q, ks, g = f64(q_t), f64(kv_sel), f64(dout_t)
+    dl = np.zeros(q.shape[0]) if dlse_t is None else f64(dlse_t)
+    z = scale * (q @ ks.T)
+    z -= z.max(axis=1, keepdims=True)
+    p = np.exp(z)
+    p /= p.sum(axis=1, keepdims=True)
+    v = ks[:, :d_v]
+    o = p @ v
+    dz = p * (g @ v.T - np.sum(g * o, axis=1)[:, None] + dl[:, None])
+    e_d = o_rel * np.sum(np.abs(g) * (p @ np.abs(v)), axis=1)
+    mag = np.abs(g) @ np.abs(v).T + np.sum(np.abs(g) * np.abs(o), axis=1)[:, None] + np.abs(dl)[:, None]
+    a = p * (e_d[:, None] + 2 * BWD_ETA * mag)
+    bq = scale * (a @ np.abs(ks)) + BWD_ETA * scale * (np.abs(dz) @ np.abs(ks))
+    bkv = scale * (a.T @ np.abs(q)) + BWD_ETA_ACC * scale * (np.abs(dz).T @ np.abs(q))
+    bkv[:, :d_v] += BWD_ETA_ACC * (p.T @ np.abs(g))
+    return bq, bkv
+
+
+def index_bwd_bounds(q_t, w_t, k_sel, g_sel):
+    """Error bounds of the GPU index-score backward of one row (listed keys k_sel [m, D_I],
+    their gradients g_sel [m]).  Decisions inside the fp32 rounding of zero may differ from
+    the fp64 oracle's: their whole term is allowed; the rest carries fp32 sum errors.
+    Returns (bound_dq [H_I, D_I], bound_dw [H_I], bound_dk [m, D_I])."""
+    q, w, ks, g = f64(q_t), f64(w_t), f64(k_sel), f64(g_sel)
+    s = q @ ks.T
+    amb = np.abs(s) <= IDX_DECISION_REL * (np.abs(q) @ np.abs(ks).T)
+    ga = np.abs(w)[:, None] * np.abs(g)[None, :]
+    on = ga * (s > 0)
+    bq = BWD_ETA * (on @ np.abs(ks)) + (ga * amb) @ np.abs(ks)
+    bw = BWD_ETA * (np.maximum(s, 0) @ np.abs(g)) + \
+        (IDX_DECISION_REL * (np.abs(q) @ np.abs(ks).T)) @ np.abs(g)
+    bk = BWD_ETA_ACC * (on.T @ np.abs(q)) + (ga * amb).T @ np.abs(q)
+    return bq, bw, bk

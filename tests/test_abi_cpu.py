@@ -159,3 +159,33 @@ def test_indexer_inputs_and_update_are_checked_on_the_host(L):
     assert L.dsa_update_indexer(ctypes.byref(p), f, f, 0, 64, f, f, f, None) == B.DSA_ERR_ARG
     assert L.dsa_update_indexer(ctypes.byref(p), f, None, 2, 64, f, f, f, None) == B.DSA_ERR_ARG
     assert L.dsa_update_indexer(ctypes.byref(p), g, f, 2, 64, f, f, f, None) == B.DSA_ERR_ARG
+
+
+def test_backward_calls_are_checked_on_the_host(L):
+    p = B.make_params(**V32)
+    P = ctypes.byref(p)
+    f = _fake()
+    g = ctypes.c_void_p(f.value + 4)   # not 16-byte aligned
+    # q, kv, idx, cu, batch, total_q, max_seqlen, out, lse, dout, dlse, dq, dkv, stream
+    ok = [f, f, f, f, 1, 8, 8, f, f, f, None, f, f, None]
+    assert L.dsa_sparse_mla_attn_bwd(None, *ok) == B.DSA_ERR_ARG
+    assert L.dsa_sparse_mla_attn_bwd(P, *ok[:8], None, *ok[9:]) == B.DSA_ERR_ARG      # lse is required
+    assert L.dsa_sparse_mla_attn_bwd(P, *ok[:11], None, *ok[12:]) == B.DSA_ERR_ARG    # dq missing
+    assert L.dsa_sparse_mla_attn_bwd(P, g, *ok[1:]) == B.DSA_ERR_ARG                  # misaligned q
+    assert L.dsa_sparse_mla_attn_bwd(P, *ok[:10], g, *ok[11:]) == B.DSA_ERR_ARG       # misaligned dlse
+    assert L.dsa_sparse_mla_attn_bwd(P, *ok[:4], 0, *ok[5:]) == B.DSA_ERR_ARG         # batch < 1
+    assert L.dsa_sparse_mla_attn_bwd(P, *ok[:5], 0, *ok[6:]) == B.DSA_OK              # nothing to do
+    wide = B.make_params(**dict(V32, d_qk=648, d_v=512))
+    assert L.dsa_sparse_mla_attn_bwd(ctypes.byref(wide), *ok) == B.DSA_ERR_UNSUPPORTED
+    big32 = B.make_params(**dict(TINY, n_heads=128, d_qk=576, d_v=512))   # fp32 tiles beyond 227 KB
+    assert L.dsa_sparse_mla_attn_bwd(ctypes.byref(big32), *ok) == B.DSA_ERR_UNSUPPORTED
+    # q_idx, w, k_idx, idx, d_scores, cu, batch, total_q, max_seqlen, dq_idx, dw, dk_idx, stream
+    ik = [f, f, f, f, f, f, 1, 8, 8, f, f, f, None]
+    assert L.dsa_index_scores_bwd(None, *ik) == B.DSA_ERR_ARG
+    assert L.dsa_index_scores_bwd(P, *ik[:4], None, *ik[5:]) == B.DSA_ERR_ARG         # d_scores missing
+    assert L.dsa_index_scores_bwd(P, *ik[:2], g, *ik[3:]) == B.DSA_ERR_ARG            # misaligned k_idx
+    assert L.dsa_index_scores_bwd(P, *ik[:7], 0, *ik[8:]) == B.DSA_OK                 # nothing to do
+    many = B.make_params(**dict(V32, n_idx_heads=128))
+    assert L.dsa_index_scores_bwd(ctypes.byref(many), *ik) == B.DSA_ERR_UNSUPPORTED
+    deep = B.make_params(**dict(V32, idx_dim=256))
+    assert L.dsa_index_scores_bwd(ctypes.byref(deep), *ik) == B.DSA_ERR_UNSUPPORTED
