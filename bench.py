@@ -916,6 +916,9 @@ def run_backward(args, cfg):
     # fp32 FMA peak of the CUDA cores: 128 lanes per SM, 2 flop per FMA, at the maximum SM clock
     alu_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
     fl = [selected * flop_per_pair_attn_bwd(cfg), selected * flop_per_pair_idx_bwd(cfg)]
+    # the DeepSeek-V3.2 shape in bf16 takes the tensor-core backward (warp-level MMAs)
+    tc_shape = (cfg.dtype == "bf16" and cfg.n_heads == 128 and cfg.d_qk == 576 and cfg.d_v == 512
+                and cfg.n_idx_heads == 64 and cfg.idx_dim == 128)
     tf = [f / (m * 1e9) for f, m in zip(fl, ms)]
     line = {
         "metric": "DSA backward (selection fixed) TFLOP/s: sparse attention + index scores",
@@ -926,16 +929,22 @@ def run_backward(args, cfg):
                    "l2": "flushed (256 MB write) between timed steps", "timing": f"median of {args.steps} steps"},
         "stages": {
             "sparse_mla_attn_bwd": {"ms": ms[0], "tflops": tf[0], "flop_per_pair": flop_per_pair_attn_bwd(cfg),
-                                    "frac_of_alu_peak": tf[0] / alu_peak,
-                                    "frac_of_bf16_peak": tf[0] / peaks["bf16_tflops"]},
+                                    "kernel": "attn_bwd_mma_kernel (bf16 mma.sync)" if tc_shape
+                                    else "attn_bwd_kernel (fp32 CUDA cores)",
+                                    "frac_of_bf16_peak": tf[0] / peaks["bf16_tflops"],
+                                    "frac_of_alu_peak": None if tc_shape else tf[0] / alu_peak},
             "index_scores_bwd": {"ms": ms[1], "tflops": tf[1], "flop_per_pair": flop_per_pair_idx_bwd(cfg),
                                  "frac_of_alu_peak": tf[1] / alu_peak,
                                  "frac_of_bf16_peak": tf[1] / peaks["bf16_tflops"]},
         },
-        "roofline": {"bound": "alu", "kernel": "attn_bwd_kernel<bf16>", "achieved": tf[0], "peak": alu_peak,
-                     "unit": "TFLOP/s", "frac": tf[0] / alu_peak,
-                     "peak_kind": f"fp32 FMA on the CUDA cores: {props.multi_processor_count} SMs x 128 lanes x 2 "
-                                  f"flop x {mhz:.0f} MHz"},
+        "roofline": ({"bound": "tensor", "kernel": "attn_bwd_mma_kernel", "achieved": tf[0],
+                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": tf[0] / peaks["bf16_tflops"],
+                      "peak_kind": f"bf16 dense, burst, {peaks['source']} (warp-level MMA, not tcgen05)"}
+                     if tc_shape else
+                     {"bound": "alu", "kernel": "attn_bwd_kernel", "achieved": tf[0], "peak": alu_peak,
+                      "unit": "TFLOP/s", "frac": tf[0] / alu_peak,
+                      "peak_kind": f"fp32 FMA on the CUDA cores: {props.multi_processor_count} SMs x 128 lanes x "
+                                   f"2 flop x {mhz:.0f} MHz"}),
         "clocks": clocks, "gpu_launches": 4 * args.steps,   # two zero fills and the two backward kernels
     }
     print(json.dumps(line), flush=True)

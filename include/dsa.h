@@ -298,8 +298,11 @@ int dsa_update_indexer(const dsa_params* params, const void* k_new, const void* 
  * top-k selection is piecewise constant in the scores, so no gradient passes
  * through it; the differentiable parts are the attention over the selected
  * positions and the index scores themselves.  The pages give no loss, so the
- * gradients of the outputs are inputs.  Both calls run on the CUDA cores in
- * fp32, accumulate the key-side gradients with fp32 atomic adds (so their
+ * gradients of the outputs are inputs.  The attention backward runs its
+ * contractions on warp-level bf16 tensor-core MMAs (fp32 accumulation; p and dz
+ * rounded to bf16 as operands) at the DeepSeek-V3.2 shape in bf16 and in fp32
+ * on the CUDA cores otherwise; the index backward runs on the CUDA cores in
+ * fp32.  Both accumulate the key-side gradients with fp32 atomic adds (so their
  * summation order, and the last bits, vary from run to run), and write fp32
  * gradients.  Packed prefill batches only (cu_seqlens as in the forward).
  *

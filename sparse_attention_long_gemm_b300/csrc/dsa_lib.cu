@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "attn_bwd.cuh"
+#include "attn_bwd_mma.cuh"
 #include "attn_simt.cuh"
 #include "attn_tc.cuh"
 #include "gemm_tc.cuh"
@@ -123,6 +124,7 @@ int device_info(DevInfo** out) {
         d.max_smem = std::min(static_cast<size_t>(optin), kMaxDynSmem);
         set(reinterpret_cast<const void*>(&attn_bwd_kernel<float>), d.max_smem);
         set(reinterpret_cast<const void*>(&attn_bwd_kernel<__nv_bfloat16>), d.max_smem);
+        set(reinterpret_cast<const void*>(&attn_bwd_mma_kernel), abm::SMEM);
         set(reinterpret_cast<const void*>(&index_scores_bwd_kernel<float>), IbSmem<float>(kIbMaxDim).bytes);
         set(reinterpret_cast<const void*>(&index_scores_bwd_kernel<__nv_bfloat16>),
             IbSmem<__nv_bfloat16>(kIbMaxDim).bytes);
@@ -395,7 +397,8 @@ int run_zero(float* dst, long long n, cudaStream_t st) {
     return launch_status();
 }
 
-// Backward of step 4 for packed prefill rows: dkv zeroed, then one CTA per (row, 32 heads).
+// Backward of step 4 for packed prefill rows: dkv zeroed, then one CTA per (row, 32 heads); the
+// DeepSeek-V3.2 shape in bf16 runs its contractions on the tensor cores, other shapes on the CUDA cores.
 int run_attn_bwd(const dsa_params* p, const void* q, const void* kv, const int* idx, const RowSpec& rs, int rows,
                  const void* out, const float* lse, const void* dout, const float* dlse, float* dq, float* dkv,
                  cudaStream_t st) {
@@ -407,7 +410,12 @@ int run_attn_bwd(const dsa_params* p, const void* q, const void* kv, const int* 
     if (sm > di->max_smem) return DSA_ERR_UNSUPPORTED;
     if ((rc = run_zero(dkv, static_cast<long long>(rows) * p->d_qk, st)) != DSA_OK) return rc;
     const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>((p->n_heads + kAbHeads - 1) / kAbHeads));
-    if (p->dtype == DSA_BF16) {
+    if (is_tc_shape(p)) {
+        using T = __nv_bfloat16;
+        attn_bwd_mma_kernel<<<grid, abm::kThreads, abm::SMEM, st>>>(
+            rs, static_cast<const T*>(q), static_cast<const T*>(kv), idx, p->topk, p->softmax_scale,
+            static_cast<const T*>(out), lse, static_cast<const T*>(dout), dlse, dq, dkv, rows);
+    } else if (p->dtype == DSA_BF16) {
         using T = __nv_bfloat16;
         attn_bwd_kernel<T><<<grid, kAbThreads, sm, st>>>(
             rs, static_cast<const T*>(q), static_cast<const T*>(kv), idx, p->topk, p->n_heads, p->d_qk, p->d_v,

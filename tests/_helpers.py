@@ -113,18 +113,22 @@ BWD_ETA_ACC = 1e-4
 O_REL_BF16_FORWARD = 2.0 ** -8
 O_REL_BF16_ROUNDED = 2.0 ** -9
 O_REL_FP32_FORWARD = 4e-6
+# The tensor-core backward rounds p and scale * dz to bf16 before its dq / dkv products (2^-9
+# each, round to nearest even), taken with a factor 2.
+DZ_REL_BF16 = 2.0 ** -8
 # A fp32 dot product of D_I bf16 products is off by at most (D_I - 1) 2^-24 sum |q k|;
 # decisions [S > 0] with |S| inside 2e-5 sum |q k| may fall either way.
 IDX_DECISION_REL = 2e-5
 
 
-def attn_bwd_bounds(q_t, kv_sel, scale, d_v, dout_t, dlse_t, o_rel):
+def attn_bwd_bounds(q_t, kv_sel, scale, d_v, dout_t, dlse_t, o_rel, dz_rel=0.0):
     """Error bounds of the GPU backward of one query row against the fp64 oracle.
 
     q_t [H, D_qk], kv_sel [m, D_qk] (the selected rows), dout_t [H, d_v], dlse_t [H].
     The gradient dz = p (dP - D + dlse) carries: the error of D = dO . O from the forward's
     O (o_rel * sum_d |dO_d| sum_i p_i |v_id|) and the fp32 errors of dP, D and p (ETA times
-    the absolute sums).  dq and dkv add the fp32 error of their own sums.
+    the absolute sums).  dq and dkv add the fp32 error of their own sums and, with dz_rel, the
+    rounding of dz and p to the MMA operand type.
     Returns (bound_dq [H, D_qk], bound_dkv [m, D_qk])."""
     q, ks, g = f64(q_t), f64(kv_sel), f64(dout_t)
     dl = np.zeros(q.shape[0]) if dlse_t is None else f64(dlse_t)
@@ -138,9 +142,9 @@ def attn_bwd_bounds(q_t, kv_sel, scale, d_v, dout_t, dlse_t, o_rel):
     e_d = o_rel * np.sum(np.abs(g) * (p @ np.abs(v)), axis=1)
     mag = np.abs(g) @ np.abs(v).T + np.sum(np.abs(g) * np.abs(o), axis=1)[:, None] + np.abs(dl)[:, None]
     a = p * (e_d[:, None] + 2 * BWD_ETA * mag)
-    bq = scale * (a @ np.abs(ks)) + BWD_ETA * scale * (np.abs(dz) @ np.abs(ks))
-    bkv = scale * (a.T @ np.abs(q)) + BWD_ETA_ACC * scale * (np.abs(dz).T @ np.abs(q))
-    bkv[:, :d_v] += BWD_ETA_ACC * (p.T @ np.abs(g))
+    bq = scale * (a @ np.abs(ks)) + (BWD_ETA + dz_rel) * scale * (np.abs(dz) @ np.abs(ks))
+    bkv = scale * (a.T @ np.abs(q)) + (BWD_ETA_ACC + dz_rel) * scale * (np.abs(dz).T @ np.abs(q))
+    bkv[:, :d_v] += (BWD_ETA_ACC + dz_rel) * (p.T @ np.abs(g))
     return bq, bkv
 
 

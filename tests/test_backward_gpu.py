@@ -18,8 +18,8 @@ from sparse_attention_long_gemm_b300.build import build_library
 from sparse_attention_long_gemm_b300.synth import (CONFIGS, make_backward_inputs, make_prefill_inputs,
                                                    random_selection, scaled)
 
-from _helpers import (O_REL_BF16_FORWARD, O_REL_BF16_ROUNDED, O_REL_FP32_FORWARD, attn_bwd_bounds, f64,
-                      index_bwd_bounds)
+from _helpers import (DZ_REL_BF16, O_REL_BF16_FORWARD, O_REL_BF16_ROUNDED, O_REL_FP32_FORWARD, attn_bwd_bounds,
+                      f64, index_bwd_bounds)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -54,7 +54,7 @@ def _oracle_forward(q, kv, idx, cu, scale, d_v):
     return out, lse
 
 
-def _attn_case(cfg, seed, qmul=1.0, rows=None, oracle_out=False, o_rel=None):
+def _attn_case(cfg, seed, qmul=1.0, rows=None, oracle_out=False, o_rel=None, dz_rel=0.0):
     inp = make_prefill_inputs(cfg, DEV, seed=seed)
     q, kv, cu = inp["q"], inp["kv"], inp["cu_seqlens"]
     if qmul != 1.0:   # larger logits: peaked softmax rows
@@ -96,7 +96,7 @@ def _attn_case(cfg, seed, qmul=1.0, rows=None, oracle_out=False, o_rel=None):
         lo = cul[seq_of[i]]
         sel = ix[r][ix[r] >= 0]
         bq, bk = attn_bwd_bounds(f64(qc[r]), kvn[lo + sel], cfg.softmax_scale, cfg.d_v, f64(gc[r]), f64(dlc[r]),
-                                 o_rel)
+                                 o_rel, dz_rel)
         err = np.abs(dq_g[i] - ref["dq"][i])
         bad = np.argwhere(err > bq + 1e-30)
         assert bad.size == 0, f"row {r}: dq off at {bad[:4].tolist()}: err {err[tuple(bad[0])]:.3e} > " \
@@ -110,24 +110,33 @@ def _attn_case(cfg, seed, qmul=1.0, rows=None, oracle_out=False, o_rel=None):
 
 
 def test_attn_bwd_tiny_fp32():
-    """fp32, 8 heads of 80/64, k = 64, two sequences: several selection blocks, a ragged tail."""
+    """fp32, 8 heads of 80/64, k = 64, two sequences: several selection blocks, a ragged tail
+    (CUDA-core kernel)."""
     cfg = scaled(CONFIGS["tiny"], seqlens=(100, 157))
     _attn_case(cfg, seed=1, o_rel=O_REL_FP32_FORWARD)
 
 
+def test_attn_bwd_bf16_general_shape():
+    """bf16 with 48 heads (not the tensor-core shape): the CUDA-core kernel in bf16, a head group
+    of 16 heads beyond the first 32, k = 64 over two sequences; out and lse from the general
+    forward (fp32 arithmetic, bf16 output)."""
+    cfg = scaled(CONFIGS["v32"], seqlens=(90, 131), topk=64, n_heads=48)
+    _attn_case(cfg, seed=6, o_rel=O_REL_BF16_ROUNDED + O_REL_FP32_FORWARD)
+
+
 @pytest.mark.parametrize("qmul", [1.0, 12.0])
 def test_attn_bwd_v32_shape_after_tensor_core_forward(qmul):
-    """DeepSeek-V3.2 dims (128 heads, 576/512, bf16), k = 96 over two sequences; out and lse
-    from the tensor-core forward; qmul = 12 makes the softmax rows peaked."""
+    """DeepSeek-V3.2 dims (128 heads, 576/512, bf16: the tensor-core backward), k = 96 over two
+    sequences; out and lse from the tensor-core forward; qmul = 12 makes the softmax rows peaked."""
     cfg = scaled(CONFIGS["v32"], seqlens=(150, 229), topk=96)
-    _attn_case(cfg, seed=2, qmul=qmul, o_rel=O_REL_BF16_FORWARD)
+    _attn_case(cfg, seed=2, qmul=qmul, o_rel=O_REL_BF16_FORWARD, dz_rel=DZ_REL_BF16)
 
 
 def test_attn_bwd_isolated_dense_causal():
     """k >= L (every causal position, long -1 tails, skipped blocks); out and lse from the
     oracle rounded to bf16, so only the backward kernel's arithmetic is measured."""
     cfg = scaled(CONFIGS["v32"], seqlens=(1, 70, 257), topk=2048)
-    _attn_case(cfg, seed=3, oracle_out=True, o_rel=O_REL_BF16_ROUNDED)
+    _attn_case(cfg, seed=3, oracle_out=True, o_rel=O_REL_BF16_ROUNDED, dz_rel=DZ_REL_BF16)
 
 
 def test_attn_bwd_full_size_sampled():
@@ -136,7 +145,7 @@ def test_attn_bwd_full_size_sampled():
     cfg = CONFIGS["v32"]
     L, k = 4096, cfg.topk
     rows = sorted({0, k - 2, k - 1, k, L - 1, 517, 3001})
-    dq, dkv, ref = _attn_case(cfg, seed=4, rows=rows, o_rel=O_REL_BF16_FORWARD)
+    dq, dkv, ref = _attn_case(cfg, seed=4, rows=rows, o_rel=O_REL_BF16_FORWARD, dz_rel=DZ_REL_BF16)
     others = torch.ones(L, dtype=torch.bool, device=DEV)
     others[torch.tensor(rows, device=DEV)] = False
     assert torch.count_nonzero(dq[others]).item() == 0
