@@ -917,8 +917,8 @@ def run_backward(args, cfg):
     alu_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
     fl = [selected * flop_per_pair_attn_bwd(cfg), selected * flop_per_pair_idx_bwd(cfg)]
     # the DeepSeek-V3.2 shape in bf16 takes the tensor-core backward (warp-level MMAs)
-    tc_shape = (cfg.dtype == "bf16" and cfg.n_heads == 128 and cfg.d_qk == 576 and cfg.d_v == 512
-                and cfg.n_idx_heads == 64 and cfg.idx_dim == 128)
+    idx_tc = cfg.dtype == "bf16" and cfg.n_idx_heads == 64 and cfg.idx_dim == 128
+    tc_shape = idx_tc and cfg.n_heads == 128 and cfg.d_qk == 576 and cfg.d_v == 512
     tf = [f / (m * 1e9) for f, m in zip(fl, ms)]
     line = {
         "metric": "DSA backward (selection fixed) TFLOP/s: sparse attention + index scores",
@@ -934,8 +934,10 @@ def run_backward(args, cfg):
                                     "frac_of_bf16_peak": tf[0] / peaks["bf16_tflops"],
                                     "frac_of_alu_peak": None if tc_shape else tf[0] / alu_peak},
             "index_scores_bwd": {"ms": ms[1], "tflops": tf[1], "flop_per_pair": flop_per_pair_idx_bwd(cfg),
-                                 "frac_of_alu_peak": tf[1] / alu_peak,
-                                 "frac_of_bf16_peak": tf[1] / peaks["bf16_tflops"]},
+                                 "kernel": "index_scores_bwd_mma_kernel (bf16 mma.sync)" if idx_tc
+                                 else "index_scores_bwd_kernel (fp32 CUDA cores)",
+                                 "frac_of_bf16_peak": tf[1] / peaks["bf16_tflops"],
+                                 "frac_of_alu_peak": None if idx_tc else tf[1] / alu_peak},
         },
         "roofline": ({"bound": "tensor", "kernel": "attn_bwd_mma_kernel", "achieved": tf[0],
                       "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": tf[0] / peaks["bf16_tflops"],

@@ -20,6 +20,7 @@
 #include "attn_tc.cuh"
 #include "gemm_tc.cuh"
 #include "indexer_bwd.cuh"
+#include "indexer_bwd_mma.cuh"
 #include "indexer_fp8.cuh"
 #include "indexer_simt.cuh"
 #include "indexer_tc.cuh"
@@ -125,6 +126,7 @@ int device_info(DevInfo** out) {
         set(reinterpret_cast<const void*>(&attn_bwd_kernel<float>), d.max_smem);
         set(reinterpret_cast<const void*>(&attn_bwd_kernel<__nv_bfloat16>), d.max_smem);
         set(reinterpret_cast<const void*>(&attn_bwd_mma_kernel), abm::SMEM);
+        set(reinterpret_cast<const void*>(&index_scores_bwd_mma_kernel), ibm::SMEM);
         set(reinterpret_cast<const void*>(&index_scores_bwd_kernel<float>), IbSmem<float>(kIbMaxDim).bytes);
         set(reinterpret_cast<const void*>(&index_scores_bwd_kernel<__nv_bfloat16>),
             IbSmem<__nv_bfloat16>(kIbMaxDim).bytes);
@@ -429,13 +431,20 @@ int run_attn_bwd(const dsa_params* p, const void* q, const void* kv, const int* 
     return launch_status();
 }
 
-// Backward of step 1 at listed positions for packed prefill rows: dk zeroed, then one CTA per row.
+// Backward of step 1 at listed positions for packed prefill rows: dk zeroed, then one CTA per row;
+// the DeepSeek-V3.2 indexer shape (64 x 128, bf16) runs its contractions on the tensor cores.
 int run_index_scores_bwd(const dsa_params* p, const void* q_idx, const float* w, const void* k_idx, const int* idx,
                          const float* dsc, const RowSpec& rs, int rows, float* dq, float* dw, float* dk,
                          cudaStream_t st) {
-    int rc = run_zero(dk, static_cast<long long>(rows) * p->idx_dim, st);
+    DevInfo* di = nullptr;
+    int rc = device_info(&di);
     if (rc != DSA_OK) return rc;
-    if (p->dtype == DSA_BF16) {
+    if ((rc = run_zero(dk, static_cast<long long>(rows) * p->idx_dim, st)) != DSA_OK) return rc;
+    if (fp8_shape(p)) {
+        using T = __nv_bfloat16;
+        index_scores_bwd_mma_kernel<<<rows, ibm::kThreads, ibm::SMEM, st>>>(
+            rs, static_cast<const T*>(q_idx), w, static_cast<const T*>(k_idx), idx, dsc, p->topk, dq, dw, dk, rows);
+    } else if (p->dtype == DSA_BF16) {
         using T = __nv_bfloat16;
         index_scores_bwd_kernel<T><<<rows, kIbThreads, IbSmem<T>(p->idx_dim).bytes, st>>>(
             rs, static_cast<const T*>(q_idx), w, static_cast<const T*>(k_idx), idx, dsc, p->topk, p->n_idx_heads,

@@ -148,18 +148,19 @@ def attn_bwd_bounds(q_t, kv_sel, scale, d_v, dout_t, dlse_t, o_rel, dz_rel=0.0):
     return bq, bkv
 
 
-def index_bwd_bounds(q_t, w_t, k_sel, g_sel):
+def index_bwd_bounds(q_t, w_t, k_sel, g_sel, g_rel=0.0):
     """Error bounds of the GPU index-score backward of one row (listed keys k_sel [m, D_I],
     their gradients g_sel [m]).  Decisions inside the fp32 rounding of zero may differ from
-    the fp64 oracle's: their whole term is allowed; the rest carries fp32 sum errors.
+    the fp64 oracle's: their whole term is allowed; the rest carries fp32 sum errors and, with
+    g_rel, the rounding of G = g w to the MMA operand type.
     Returns (bound_dq [H_I, D_I], bound_dw [H_I], bound_dk [m, D_I])."""
     q, w, ks, g = f64(q_t), f64(w_t), f64(k_sel), f64(g_sel)
     s = q @ ks.T
     amb = np.abs(s) <= IDX_DECISION_REL * (np.abs(q) @ np.abs(ks).T)
     ga = np.abs(w)[:, None] * np.abs(g)[None, :]
     on = ga * (s > 0)
-    bq = BWD_ETA * (on @ np.abs(ks)) + (ga * amb) @ np.abs(ks)
+    bq = (BWD_ETA + g_rel) * (on @ np.abs(ks)) + (ga * amb) @ np.abs(ks)
     bw = BWD_ETA * (np.maximum(s, 0) @ np.abs(g)) + \
         (IDX_DECISION_REL * (np.abs(q) @ np.abs(ks).T)) @ np.abs(g)
-    bk = BWD_ETA_ACC * (on.T @ np.abs(q)) + (ga * amb).T @ np.abs(q)
+    bk = (BWD_ETA_ACC + g_rel) * (on.T @ np.abs(q)) + (ga * amb).T @ np.abs(q)
     return bq, bw, bk
