@@ -60,3 +60,15 @@ def test_attn_traffic_null_after_a_source_change(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", _fake_root(tmp_path, b"// changed\n", hashlib.sha1(b"// old\n").hexdigest()))
     assert bench._attn_traffic(CONFIGS["long"]) is None
 
+
+
+def test_backward_flop_per_pair():
+    """The backward's algorithmic work per selected pair, counted term by term: per head the
+    logits (2 d_qk), dP (2 d_v), dq (2 d_qk) and dkv (2 d_qk + 2 d_v); per indexer head S, dq_I
+    and dk_I (2 D_I each)."""
+    v = CONFIGS["v32"]
+    per_head = 2 * v.d_qk + 2 * v.d_v + 2 * v.d_qk + (2 * v.d_qk + 2 * v.d_v)
+    assert bench.flop_per_pair_attn_bwd(v) == v.n_heads * per_head == 704_512
+    assert bench.flop_per_pair_idx_bwd(v) == v.n_idx_heads * 3 * 2 * v.idx_dim == 49_152
+    # 2.53 times the forward's attention work per pair (278,528)
+    assert bench.flop_per_pair_attn_bwd(v) / bench.flop_per_pair_attn(v) == pytest.approx(2.529, abs=1e-3)
